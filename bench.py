@@ -1,0 +1,376 @@
+"""Benchmark of the MoE SwiGLU FFN forward pass on GB300.
+
+A step is one forward pass of the whole layer (router -> top-k/softmax ->
+stable permutation -> W1||W3 + SiLU*mul -> W2 -> weighted combine, plus the
+shared expert) over one batch of synthetic tokens of the GPT-OSS-Lite-shaped
+workload (T=32768, D=768, F=1536, E=8 routed top-2 + 1 shared expert), with
+all inputs resident in HBM.  One JSON line is printed by rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+Timing: W untimed warm-up steps; then K steps, each bracketed by CUDA events
+on the launching stream, with a 512 MB buffer written between steps to flush
+the 129 MB L2 (outside the events).  Multi-GPU (torchrun): every rank runs its
+own replica of the layer on its own batch (weak scaling, no collective on the
+data path); the step time is the max over ranks.
+
+--impl reference times the fp64 CPU oracle as it stands on the host cores,
+on a bounded sample of the same workload, and prints the same line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from grouped_gemm_router_gb300 import inputs  # noqa: E402
+
+WORKLOAD = "gptoss_lite"
+METRIC = "MoE FFN fwd tokens/s and active TFLOP/s on 1 GB300; % of bf16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def active_flops(w) -> int:
+    """Router GEMM + routed W1/W3/W2 + shared-expert W1/W3/W2 (2 FLOPs per MAC)."""
+    return (2 * w.T * w.D * w.E + 6 * w.T * w.k * w.D * w.F
+            + (6 * w.T * w.D * w.F if w.shared else 0))
+
+
+def w1w3_flops_per_launch(w) -> int:
+    """Algorithmic FLOPs of one launch of the W1||W3 grouped GEMM: each routed
+    slot and (with the shared expert) each token does two [D]x[D,F] products."""
+    rows = w.T * w.k + (w.T if w.shared else 0)
+    return 4 * rows * w.D * w.F
+
+
+def stage_bytes(w) -> dict:
+    """Algorithmic HBM bytes per stage (each tensor read or written once)."""
+    T, D, F, E, k = w.T, w.D, w.F, w.E, w.k
+    S = T * k
+    rows = S + (T if w.shared else 0)
+    sh = 1 if w.shared else 0
+    return {
+        "route": T * D * 2 + D * E * 2 + S * 8,
+        "permute": T * D * 2 + S * D * 2 + S * 4 * 3,
+        "w1w3": S * D * 2 + sh * T * D * 2 + (E + sh) * 2 * D * F * 2 + rows * F * 2,
+        "w2": rows * F * 2 + (E + sh) * F * D * 2 + rows * D * 2,
+        "combine": S * D * 2 + sh * T * D * 2 + T * D * 2 + S * 8,
+    }
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "grouped_gemm_router_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when the kernels changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("source_hash") != source_hash():
+        return None
+    v = d.get("kernels", {}).get(kernel)
+    return None if v is None else float(v)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *a):
+        pass
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def to_dev(a, dev):
+    import torch
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(a).to(dev)
+
+
+def time_oracle(L, w, budget_s=12.0):
+    """Times the fp64 oracle on the first n tokens of the workload, growing n
+    until one run takes about a second, then repeats within the budget.
+    Returns (tokens/s, n tokens per run, runs, seconds)."""
+    from oracle import moe_oracle as orc
+    n = 64
+    while True:
+        t0 = time.perf_counter()
+        orc.moe_ffn_forward(L["x"][:n], L["Wg"], L["W1"], L["W3"], L["W2"], w.k, bias=L["bias"],
+                            Ws1=L["Ws1"], Ws3=L["Ws3"], Ws2=L["Ws2"])
+        dt = time.perf_counter() - t0
+        if dt > 1.0 or n >= w.T:
+            break
+        n = min(w.T, n * 4)
+    runs, total, t_start = 0, 0.0, time.perf_counter()
+    while time.perf_counter() - t_start < budget_s - dt or runs == 0:
+        t0 = time.perf_counter()
+        orc.moe_ffn_forward(L["x"][:n], L["Wg"], L["W1"], L["W3"], L["W2"], w.k, bias=L["bias"],
+                            Ws1=L["Ws1"], Ws3=L["Ws3"], Ws2=L["Ws2"])
+        total += time.perf_counter() - t0
+        runs += 1
+    return n * runs / total, n, runs, total
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return
+    L = inputs.make_layer(w)
+    # warm-up runs (not timed), then `steps` timed runs on a bounded sample
+    from oracle import moe_oracle as orc
+    n = max(64, min(w.T, 1024))
+    for _ in range(min(args.warmup, 1)):
+        orc.moe_ffn_forward(L["x"][:64], L["Wg"], L["W1"], L["W3"], L["W2"], w.k, bias=L["bias"],
+                            Ws1=L["Ws1"], Ws3=L["Ws3"], Ws2=L["Ws2"])
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        orc.moe_ffn_forward(L["x"][:n], L["Wg"], L["W1"], L["W3"], L["W2"], w.k, bias=L["bias"],
+                            Ws1=L["Ws1"], Ws3=L["Ws3"], Ws2=L["Ws2"])
+        times.append(time.perf_counter() - t0)
+        if sum(times) > 120:
+            break
+    tps = n * len(times) / sum(times)
+    sample = f"first {n} of {w.T} tokens per step through the whole layer (fp64 numpy oracle)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 * w.T / tps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "T": w.T, "D": w.D, "F": w.F, "E": w.E,
+                                        "k": w.k, "shared_expert": w.shared},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD, choices=list(inputs.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "native":
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = inputs.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    from grouped_gemm_router_gb300 import build
+    build.build()
+    from grouped_gemm_router_gb300 import moe
+
+    L = inputs.make_layer(w)
+    G = {k: to_dev(v, dev) for k, v in L.items()}
+    T, D, F, E, k = w.T, w.D, w.F, w.E, w.k
+    ws = moe.Workspace(T, D, F, E, k, w.shared, device=dev)
+    out = torch.empty(T, D, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step(events=None):
+        moe.moe_ffn_forward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], k, bias=G["bias"],
+                            Ws1=G["Ws1"], Ws3=G["Ws3"], Ws2=G["Ws2"], out=out, workspace=ws,
+                            stage_events=events)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if moe.device_error() != 0:
+        raise RuntimeError("device wait timed out during warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank).__enter__()
+    n_launch0 = moe.launch_count()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    n_launch = moe.launch_count() - n_launch0
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    if moe.device_error() != 0:
+        raise RuntimeError("device wait timed out during the timed steps")
+
+    stage_ms = np.array([[evs[i][s].elapsed_time(evs[i][s + 1]) for s in range(5)] for i in range(K)])
+    step_ms = np.array([evs[i][0].elapsed_time(evs[i][5]) for i in range(K)])
+    ms = float(step_ms.mean())
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end through the host-memory entry point ----
+    ws_h = moe.Workspace(T, D, F, E, k, w.shared, host_io=True, device=dev)
+    x_host = G["x"].cpu().pin_memory()
+    out_host = torch.empty(T, D, dtype=torch.bfloat16).pin_memory()
+    K2 = max(3, min(K, 50))
+    e2e_ms = []
+    for i in range(args.warmup + K2):
+        ev = [None] * 8
+        ev[6], ev[7] = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.zero_()
+        moe.moe_ffn_forward_host(x_host, G["Wg"], G["W1"], G["W3"], G["W2"], k, out_host, ws_h,
+                                 bias=G["bias"], Ws1=G["Ws1"], Ws3=G["Ws3"], Ws2=G["Ws2"],
+                                 stage_events=ev)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(ev[6].elapsed_time(ev[7]))
+    e2e = float(np.mean(e2e_ms))
+    if world > 1:
+        t = torch.tensor([e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e = float(t.item())
+
+    pk, pk_kind = peaks()
+    names = ["route", "permute", "w1w3", "w2", "combine"]
+    st_mean = {n: float(stage_ms[:, i].mean()) for i, n in enumerate(names)}
+    sb = stage_bytes(w)
+    fl = active_flops(w)
+    tokens_s = T * world / (ms / 1e3)
+    w1w3_s = st_mean["w1w3"] / 1e3
+    achieved = w1w3_flops_per_launch(w) / w1w3_s / 1e12
+    traffic = ncu_traffic("grouped_gemm_kernel<true>")
+    hbm_stages = st_mean["route"] + st_mean["permute"] + st_mean["combine"]
+    hbm_bytes = sb["route"] + sb["permute"] + sb["combine"]
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        tps, n, runs, secs = time_oracle(L, w)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"{runs} runs of the first {n} of {w.T} tokens through the whole layer "
+                         f"({secs:.1f} s of fp64 numpy oracle)"}
+    line = {
+        "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "D": w.D, "F": w.F, "E": w.E, "k": w.k,
+                   "shared_expert": w.shared, "l2": "flushed between steps (512 MB write)",
+                   "parallelism": f"replicas x{world}"},
+        "active_tflops": fl * world / (ms / 1e3) / 1e12,
+        "frac_of_bf16_peak": fl / (ms / 1e3) / 1e12 / pk["bf16_tflops"],
+        "stage_ms": st_mean,
+        "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel<true> (W1||W3 + SiLU*mul)",
+                     "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
+                     "peak_kind": f"{pk_kind} bf16 burst"},
+        "hbm_stages": {"kernels": "route + permute + combine", "bytes": hbm_bytes, "ms": hbm_stages,
+                       "achieved_gbs": hbm_bytes / (hbm_stages / 1e3) / 1e9,
+                       "frac": hbm_bytes / (hbm_stages / 1e3) / 1e9 / pk["hbm_gbs"]},
+        "e2e": {"value": T * world / (e2e / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 2},
+        "gpu_launches": int(n_launch),
+        "clocks": clocks,
+        "wall_s_timed_loop": wall,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,41 @@
+// Host-side launchers shared between the translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_ffn.h"
+
+namespace moe {
+
+// Counts kernel launches (moe_launch_count).
+void note_launch();
+
+// ---- routing / permutation (route_permute.cu) ----
+int route_blocks(int T);  // ceil(T / MOE_ROUTE_BLOCK_TOKENS)
+cudaError_t launch_route(const uint16_t* x, const uint16_t* Wg, const float* bias, const moe_dims& d,
+                         int32_t* ids, float* w, int32_t* hist, cudaStream_t s);
+cudaError_t launch_hist(const int32_t* ids, const moe_dims& d, int32_t* hist, cudaStream_t s);
+cudaError_t launch_scatter(const int32_t* ids, const int32_t* hist, const moe_dims& d, int32_t* counts,
+                           int32_t* offsets, int32_t* perm, int32_t* inv, const uint16_t* x,
+                           uint16_t* x_sorted, cudaStream_t s);
+
+// ---- combine (combine.cu) ----
+cudaError_t launch_combine(const uint16_t* y, const float* w, const int32_t* inv, const moe_dims& d,
+                           int has_shared, uint16_t* out, cudaStream_t s);
+
+// ---- grouped GEMMs (grouped_gemm.cu) ----
+// W1||W3 with SwiGLU epilogue: A = x_sorted [S, D] (+ x [T, D] for the shared
+// group), B = W1/W3 [E, D, F] (+ Ws1/Ws3 [D, F]), C = h [S (+T), F].
+cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, const uint16_t* W1,
+                                  const uint16_t* W3, const uint16_t* Ws1, const uint16_t* Ws3,
+                                  const int32_t* offsets, const moe_dims& d, uint16_t* h,
+                                  cudaStream_t s);
+// W2: A = h [S (+T), F], B = W2 [E, F, D] (+ Ws2 [F, D]), C = y [S (+T), D].
+cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uint16_t* Ws2,
+                                const int32_t* offsets, const moe_dims& d, uint16_t* y,
+                                cudaStream_t s);
+// Reads and clears the device error word (synchronous).
+cudaError_t read_clear_device_error(unsigned int* value);
+
+}  // namespace moe

@@ -1,0 +1,368 @@
+// Router GEMM + top-k + softmax, and the stable expert-grouped permutation.
+//
+// Sources: "Chinchilla scaling, MoE, and fused Triton kernels", section
+// "PyTorch MoE implementation" (logits = x . gate_w, top-k, softmax over the
+// selected logits, stable argsort of the flattened ids, bincount, gather);
+// "Triton MoE Kernels & Memory Checkpointing", Part A, section 10.3, steps
+// 1-2 (sort-by-expert layout, counts and offsets as a cumulative sum).
+//
+// Both kernels read activations once from HBM with 16-byte loads; the router
+// GEMM (N = E, a few experts wide) runs on warp-level bf16 MMA because it is
+// far too narrow for a tcgen05 tile and the kernel is bound by reading x.
+#include <math.h>
+
+#include "moe_device.cuh"
+#include "moe_kernels.cuh"
+
+namespace moe {
+
+constexpr int kRouteTokens = MOE_ROUTE_BLOCK_TOKENS;  // tokens per block
+constexpr int kRouteWarps = kRouteTokens / 16;        // one 16-token MMA tile per warp
+constexpr int kRouteSmemBytes = 64 * 1024;            // staged router weights per D-chunk
+
+int route_blocks(int T) { return (T + kRouteTokens - 1) / kRouteTokens; }
+
+MOE_DEV void mma_m16n8k16_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Block = 4 warps = 64 tokens.  Warp w owns tokens [t0, t0 + 16).  Lane
+// (g = lane / 4, c = lane % 4) loads 16 bytes of rows g and g + 8 at columns
+// d + 8c .. d + 8c + 7 of every 32-wide chunk: a coalesced 64-byte segment per
+// row.  The reduction order over d inside a chunk is irrelevant, so those 8
+// columns feed two m16n8k16 MMAs as their (2c, 2c+1, 2c+8, 2c+9) columns, and
+// the router weights are staged in shared memory in the matching order:
+// wpack[chunk][expert tile][lane] = Wg[32 chunk + 8c + 0..7][8 tile + g].
+//
+// Selection: thread (g, c) holds the logits of experts 8n + 2c + {0,1} for
+// rows g and g + 8.  Each of the k rounds takes the largest not-yet-chosen
+// logit (ties to the lower expert index) across the quad.
+template <int NT>
+__global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ Wg, const float* __restrict__ bias,
+    int T, int D, int E, int k, int dchunk, int32_t* __restrict__ ids, float* __restrict__ wts,
+    int32_t* __restrict__ hist) {
+  extern __shared__ __align__(16) uint8_t route_smem[];
+  uint4* wpack = reinterpret_cast<uint4*>(route_smem);
+  uint16_t* wpack16 = reinterpret_cast<uint16_t*>(route_smem);
+  __shared__ int s_hist[MOE_MAX_EXPERTS];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int t0 = blockIdx.x * kRouteTokens + warp * 16;
+  const int row0 = t0 + g, row1 = t0 + g + 8;
+  const bool ok0 = row0 < T, ok1 = row1 < T;
+  const uint4* xr0 = reinterpret_cast<const uint4*>(x + static_cast<size_t>(ok0 ? row0 : 0) * D);
+  const uint4* xr1 = reinterpret_cast<const uint4*>(x + static_cast<size_t>(ok1 ? row1 : 0) * D);
+
+  for (int i = threadIdx.x; i < E; i += blockDim.x) s_hist[i] = 0;
+
+  float acc[NT][4];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+
+  constexpr int EP = NT * 8;  // experts padded to whole MMA tiles
+  for (int d0 = 0; d0 < D; d0 += dchunk) {
+    const int dc = min(dchunk, D - d0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < dc * EP; i += blockDim.x) {
+      const int dd = i / EP, e = i - dd * EP;
+      const uint16_t v = (e < E) ? Wg[static_cast<size_t>(d0 + dd) * E + e] : uint16_t(0);
+      const int kc = dd >> 5, r = dd & 31;
+      const int ln = (e & 7) * 4 + (r >> 3);
+      wpack16[((static_cast<size_t>(kc) * NT + (e >> 3)) * 32 + ln) * 8 + (r & 7)] = v;
+    }
+    __syncthreads();
+    const int nkc = dc >> 5;
+#pragma unroll 4
+    for (int kc = 0; kc < nkc; ++kc) {
+      const int q = ((d0 + kc * 32) >> 3) + c;  // 16-byte column index
+      const uint4 a0 = ok0 ? __ldg(xr0 + q) : make_uint4(0, 0, 0, 0);
+      const uint4 a1 = ok1 ? __ldg(xr1 + q) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        const uint4 b = wpack[(static_cast<size_t>(kc) * NT + n) * 32 + lane];
+        mma_m16n8k16_bf16(acc[n], a0.x, a1.x, a0.y, a1.y, b.x, b.y);
+        mma_m16n8k16_bf16(acc[n], a0.z, a1.z, a0.w, a1.w, b.z, b.w);
+      }
+    }
+  }
+
+  // ---- top-k + softmax for rows g (r = 0) and g + 8 (r = 1) ----
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int row = r ? row1 : row0;
+    float v[2 * NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = n * 8 + 2 * c + h;
+        float l = acc[n][2 * r + h];
+        if (bias != nullptr && e < E) l += bias[e];
+        if (isnan(l)) l = -INFINITY;
+        v[2 * n + h] = l;
+      }
+    }
+    uint32_t taken = 0;
+    float sel_v[MOE_MAX_TOPK];
+    int sel_e[MOE_MAX_TOPK];
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+      sel_v[j] = 0.f;
+      sel_e[j] = 0;
+      if (j < k) {
+        float best = -INFINITY;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < 2 * NT; ++i) {
+          const int e = (i >> 1) * 8 + 2 * c + (i & 1);
+          if (e < E && !((taken >> i) & 1u) && (v[i] > best || (v[i] == best && e < be))) {
+            best = v[i];
+            be = e;
+          }
+        }
+#pragma unroll
+        for (int off = 1; off <= 2; off <<= 1) {
+          const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+          if (ob > best || (ob == best && oe < be)) {
+            best = ob;
+            be = oe;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 2 * NT; ++i) {
+          const int e = (i >> 1) * 8 + 2 * c + (i & 1);
+          if (e == be) taken |= 1u << i;
+        }
+        sel_v[j] = best;
+        sel_e[j] = be;
+      }
+    }
+    float z[MOE_MAX_TOPK];
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+      z[j] = 0.f;
+      if (j < k) {
+        z[j] = expf(sel_v[j] - sel_v[0]);
+        sum += z[j];
+      }
+    }
+    if (row < T) {
+#pragma unroll
+      for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+        if (j < k && (j & 3) == c) {
+          ids[static_cast<size_t>(row) * k + j] = sel_e[j];
+          wts[static_cast<size_t>(row) * k + j] = z[j] / sum;
+          atomicAdd(&s_hist[sel_e[j]], 1);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (hist != nullptr)
+    for (int i = threadIdx.x; i < E; i += blockDim.x)
+      hist[static_cast<size_t>(blockIdx.x) * E + i] = s_hist[i];
+}
+
+// Per-block expert histogram of given ids (same blocking as route_kernel).
+__global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ ids, int T, int k,
+                                                   int E, int32_t* __restrict__ hist) {
+  __shared__ int s_hist[MOE_MAX_EXPERTS];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) s_hist[i] = 0;
+  __syncthreads();
+  const int s0 = blockIdx.x * kRouteTokens * k;  // T * k <= 2^28 fits in int
+  const int ns = min(kRouteTokens * k, T * k - s0);
+  for (int i = threadIdx.x; i < ns; i += blockDim.x) atomicAdd(&s_hist[ids[s0 + i]], 1);
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x)
+    hist[static_cast<size_t>(blockIdx.x) * E + i] = s_hist[i];
+}
+
+// Scatter: block b owns the slots of tokens [64b, 64b + 64).
+//  1. From the whole block histogram it forms counts, offsets (exclusive
+//     scan over experts) and this block's first position per expert
+//     (offsets[e] + the counts of expert e in blocks before b).
+//  2. Slots are ranked stably in rounds of 256 (one per thread): within a
+//     warp by __match_any_sync, across warps by per-warp counts.
+//  3. perm/inv are written and x rows are copied to x_sorted with 16-byte
+//     vector loads and stores, one warp per row.
+constexpr int kScatterThreads = 256;
+constexpr int kScatterWarps = kScatterThreads / 32;
+
+__global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
+    const int32_t* __restrict__ ids, const int32_t* __restrict__ hist, int T, int k, int E, int nblk,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv, const uint4* __restrict__ x, uint4* __restrict__ xs, int D) {
+  __shared__ int s_red_pre[kScatterThreads];
+  __shared__ int s_red_tot[kScatterThreads];
+  __shared__ int s_base[MOE_MAX_EXPERTS];
+  __shared__ int s_wcnt[kScatterWarps][MOE_MAX_EXPERTS];
+  __shared__ int s_pos[kRouteTokens * MOE_MAX_TOPK];
+
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = T * k;
+
+  // ---- 1. column sums of the block histogram ----
+  {
+    const int R = kScatterThreads / E;  // E <= 128 -> R >= 2
+    const int e = tid % E, r = tid / E;
+    int pre = 0, tot = 0;
+    if (r < R) {
+      for (int bb = r; bb < nblk; bb += R) {
+        const int hv = hist[static_cast<size_t>(bb) * E + e];
+        tot += hv;
+        if (bb < b) pre += hv;
+      }
+    }
+    s_red_pre[tid] = pre;
+    s_red_tot[tid] = tot;
+    __syncthreads();
+    if (warp == 0) {
+      // lane handles experts [lane*per, lane*per + per)
+      const int per = (E + 31) / 32;
+      int tot_e[4], pre_e[4];
+      int local = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        tot_e[i] = pre_e[i] = 0;
+        const int ee = lane * per + i;
+        if (i < per && ee < E) {
+          for (int rr = 0; rr < R; ++rr) {
+            tot_e[i] += s_red_tot[rr * E + ee];
+            pre_e[i] += s_red_pre[rr * E + ee];
+          }
+          local += tot_e[i];
+        }
+      }
+      int incl = local;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      int run = incl - local;  // exclusive prefix of this lane's first expert
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int ee = lane * per + i;
+        if (i < per && ee < E) {
+          s_base[ee] = run + pre_e[i];
+          if (b == 0) {
+            counts[ee] = tot_e[i];
+            offsets[ee] = run;
+          }
+          run += tot_e[i];
+        }
+      }
+      if (b == 0 && lane == 0) offsets[E] = S;
+    }
+  }
+
+  // ---- 2. stable ranks ----
+  const int s0 = b * kRouteTokens * k;
+  const int ns = min(kRouteTokens * k, S - s0);
+  for (int base = 0; base < ns; base += kScatterThreads) {
+    for (int i = tid; i < kScatterWarps * E; i += kScatterThreads) s_wcnt[i / E][i % E] = 0;
+    __syncthreads();
+    const int li = base + tid;
+    const bool valid = li < ns;
+    const int ex = valid ? ids[s0 + li] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, ex);
+    const unsigned lt = (1u << lane) - 1u;
+    const int rank = __popc(peers & lt);
+    if (valid && (__ffs(peers) - 1) == lane) s_wcnt[warp][ex] = __popc(peers);
+    __syncthreads();
+    if (valid) {
+      int pos = s_base[ex] + rank;
+      for (int w = 0; w < warp; ++w) pos += s_wcnt[w][ex];
+      perm[pos] = s0 + li;
+      inv[s0 + li] = pos;
+      s_pos[li] = pos;
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kScatterThreads) {
+      int add = 0;
+      for (int w = 0; w < kScatterWarps; ++w) add += s_wcnt[w][e];
+      s_base[e] += add;
+    }
+    __syncthreads();
+  }
+
+  // ---- 3. gather rows ----
+  if (x == nullptr) return;
+  const int n16 = D >> 3;  // 16-byte vectors per row
+  for (int i = warp; i < ns; i += kScatterWarps) {
+    const uint4* src = x + static_cast<size_t>((s0 + i) / k) * n16;
+    uint4* dst = xs + static_cast<size_t>(s_pos[i]) * n16;
+    int cidx = lane;
+    for (; cidx + 96 < n16; cidx += 128) {
+      const uint4 v0 = __ldg(src + cidx), v1 = __ldg(src + cidx + 32);
+      const uint4 v2 = __ldg(src + cidx + 64), v3 = __ldg(src + cidx + 96);
+      dst[cidx] = v0;
+      dst[cidx + 32] = v1;
+      dst[cidx + 64] = v2;
+      dst[cidx + 96] = v3;
+    }
+    for (; cidx < n16; cidx += 32) dst[cidx] = __ldg(src + cidx);
+  }
+}
+
+template <int NT>
+static cudaError_t launch_route_nt(const uint16_t* x, const uint16_t* Wg, const float* bias,
+                                  const moe_dims& d, int32_t* ids, float* w, int32_t* hist,
+                                  cudaStream_t s) {
+  int dchunk = kRouteSmemBytes / (NT * 8 * 2);
+  dchunk = (dchunk / 32) * 32;
+  if (dchunk > d.D) dchunk = d.D;
+  const size_t smem = static_cast<size_t>(dchunk) * NT * 8 * 2;
+  cudaError_t e = cudaFuncSetAttribute(route_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  route_kernel<NT><<<route_blocks(d.T), kRouteWarps * 32, smem, s>>>(x, Wg, bias, d.T, d.D, d.E, d.k,
+                                                                     dchunk, ids, w, hist);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route(const uint16_t* x, const uint16_t* Wg, const float* bias, const moe_dims& d,
+                         int32_t* ids, float* w, int32_t* hist, cudaStream_t s) {
+  const int nt = (d.E + 7) / 8;
+  switch (nt) {
+    case 1: return launch_route_nt<1>(x, Wg, bias, d, ids, w, hist, s);
+    case 2: return launch_route_nt<2>(x, Wg, bias, d, ids, w, hist, s);
+    case 3:
+    case 4: return launch_route_nt<4>(x, Wg, bias, d, ids, w, hist, s);
+    case 5:
+    case 6:
+    case 7:
+    case 8: return launch_route_nt<8>(x, Wg, bias, d, ids, w, hist, s);
+    default: return launch_route_nt<16>(x, Wg, bias, d, ids, w, hist, s);
+  }
+}
+
+cudaError_t launch_hist(const int32_t* ids, const moe_dims& d, int32_t* hist, cudaStream_t s) {
+  hist_kernel<<<route_blocks(d.T), 256, 0, s>>>(ids, d.T, d.k, d.E, hist);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const int32_t* ids, const int32_t* hist, const moe_dims& d, int32_t* counts,
+                           int32_t* offsets, int32_t* perm, int32_t* inv, const uint16_t* x,
+                           uint16_t* x_sorted, cudaStream_t s) {
+  const int nblk = route_blocks(d.T);
+  scatter_kernel<<<nblk, kScatterThreads, 0, s>>>(ids, hist, d.T, d.k, d.E, nblk, counts, offsets, perm,
+                                                  inv, reinterpret_cast<const uint4*>(x),
+                                                  reinterpret_cast<uint4*>(x_sorted), d.D);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

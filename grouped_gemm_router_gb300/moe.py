@@ -1,0 +1,250 @@
+"""PyTorch-facing entry points of the MoE SwiGLU FFN forward pass.
+
+These functions only allocate outputs with torch, check shapes/dtypes, and
+call the C ABI of libmoeffn.so on the current CUDA stream.  Tensor layouts:
+  x [T, D] bf16, Wg [D, E] bf16, bias [E] fp32 (optional),
+  W1, W3 [E, D, F] bf16, W2 [E, F, D] bf16,
+  shared expert Ws1, Ws3 [D, F], Ws2 [F, D] bf16 (optional).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _native as N
+from ._native import check, lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need(t, name, dtype, shape=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def layer_dims(x, W1, k):
+    T, D = x.shape
+    E, _, F = W1.shape
+    return T, D, F, E, k
+
+
+def workspace_size(T, D, F, E, k, shared, host_io=False) -> int:
+    n = lib.moe_ffn_workspace_size(N.dims(T, D, F, E, k), int(bool(shared)), int(bool(host_io)))
+    if n == 0:
+        raise N.MoeError(N.MOE_ERR_UNSUPPORTED_SHAPE, "moe_ffn_workspace_size")
+    return n
+
+
+class Workspace:
+    """Device workspace of moe_ffn_forward, with typed views of its regions
+    (the layout documented in moe_ffn.h)."""
+
+    def __init__(self, T, D, F, E, k, shared, host_io=False, device=None):
+        self.dims = (T, D, F, E, k)
+        self.shared = bool(shared)
+        self.nbytes = workspace_size(T, D, F, E, k, shared, host_io)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+
+    def views(self):
+        T, D, F, E, k = self.dims
+        S = T * k
+        rows = S + (T if self.shared else 0)
+        nblk = (T + N.ROUTE_BLOCK_TOKENS - 1) // N.ROUTE_BLOCK_TOKENS
+        out, off = {}, 0
+
+        def take(name, n, dtype, shape):
+            nonlocal off
+            size = n * torch.tensor([], dtype=dtype).element_size()
+            out[name] = self.buf[off:off + size].view(dtype).view(*shape)
+            off += (size + 255) // 256 * 256
+
+        take("ids", S, torch.int32, (T, k))
+        take("w", S, torch.float32, (T, k))
+        take("hist", nblk * E, torch.int32, (nblk, E))
+        take("counts", E, torch.int32, (E,))
+        take("offsets", E + 1, torch.int32, (E + 1,))
+        take("perm", S, torch.int32, (S,))
+        take("inv", S, torch.int32, (S,))
+        take("x_sorted", S * D, torch.bfloat16, (S, D))
+        take("h", rows * F, torch.bfloat16, (rows, F))
+        take("y", rows * D, torch.bfloat16, (rows, D))
+        return out
+
+
+def _options(stage_events=None, ids_in=None, weights_in=None):
+    if stage_events is None and ids_in is None:
+        return None
+    o = N.MoeOptions()
+    for i, ev in enumerate(stage_events or []):
+        if ev is None:
+            continue
+        handle = ev.cuda_event if hasattr(ev, "cuda_event") else int(ev)
+        if not handle:
+            # torch creates the CUDA event lazily, on its first record()
+            ev.record()
+            handle = ev.cuda_event
+        o.stage_events[i] = handle
+    if ids_in is not None:
+        _need(ids_in, "ids_in", torch.int32)
+        _need(weights_in, "weights_in", torch.float32)
+        o.ids_in = ids_in.data_ptr()
+        o.weights_in = weights_in.data_ptr()
+    return ctypes.byref(o)
+
+
+def moe_ffn_forward(x, Wg, W1, W3, W2, k, bias=None, Ws1=None, Ws3=None, Ws2=None, out=None,
+                    workspace: Workspace | None = None, stage_events=None, ids_in=None,
+                    weights_in=None):
+    """Forward pass of the MoE SwiGLU FFN layer; returns out [T, D] bf16."""
+    T, D, F, E, k = layer_dims(x, W1, k)
+    shared = Ws1 is not None
+    for t, n, shp in ((x, "x", (T, D)), (Wg, "Wg", (D, E)), (W1, "W1", (E, D, F)),
+                      (W3, "W3", (E, D, F)), (W2, "W2", (E, F, D)), (Ws1, "Ws1", (D, F)),
+                      (Ws3, "Ws3", (D, F)), (Ws2, "Ws2", (F, D))):
+        _need(t, n, torch.bfloat16, shp)
+    _need(bias, "bias", torch.float32, (E,))
+    if out is None:
+        out = torch.empty(T, D, dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = Workspace(T, D, F, E, k, shared, device=x.device)
+    st = lib.moe_ffn_forward(_ptr(x), _ptr(Wg), _ptr(bias), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(Ws1),
+                             _ptr(Ws3), _ptr(Ws2), N.dims(T, D, F, E, k), _ptr(out),
+                             _ptr(workspace.buf), workspace.nbytes,
+                             _options(stage_events, ids_in, weights_in), _stream())
+    check(st, "moe_ffn_forward")
+    return out
+
+
+def moe_ffn_forward_host(x_host, Wg, W1, W3, W2, k, out_host, workspace: Workspace, bias=None,
+                         Ws1=None, Ws3=None, Ws2=None, stage_events=None):
+    """Forward pass with x and out in (pinned) host memory; copies are part of
+    the call, enqueued on the current stream."""
+    T, D, F, E, k = layer_dims(x_host, W1, k)
+    if x_host.is_cuda or out_host.is_cuda:
+        raise ValueError("x_host and out_host must be host tensors")
+    st = lib.moe_ffn_forward_host(_ptr(x_host), _ptr(Wg), _ptr(bias), _ptr(W1), _ptr(W3), _ptr(W2),
+                                  _ptr(Ws1), _ptr(Ws3), _ptr(Ws2), N.dims(T, D, F, E, k),
+                                  _ptr(out_host), _ptr(workspace.buf), workspace.nbytes,
+                                  _options(stage_events), _stream())
+    check(st, "moe_ffn_forward_host")
+    return out_host
+
+
+def moe_route(x, Wg, k, bias=None):
+    """Router GEMM + top-k + softmax -> (ids [T,k] int32, weights [T,k] fp32,
+    block_hist [ceil(T/64), E] int32)."""
+    T, D = x.shape
+    E = Wg.shape[1]
+    _need(x, "x", torch.bfloat16, (T, D))
+    _need(Wg, "Wg", torch.bfloat16, (D, E))
+    _need(bias, "bias", torch.float32, (E,))
+    ids = torch.empty(T, k, dtype=torch.int32, device=x.device)
+    w = torch.empty(T, k, dtype=torch.float32, device=x.device)
+    nblk = (T + N.ROUTE_BLOCK_TOKENS - 1) // N.ROUTE_BLOCK_TOKENS
+    hist = torch.empty(nblk, E, dtype=torch.int32, device=x.device)
+    st = lib.moe_route(_ptr(x), _ptr(Wg), _ptr(bias), N.dims(T, D, 64, E, k), _ptr(ids), _ptr(w),
+                       _ptr(hist), _stream())
+    check(st, "moe_route")
+    return ids, w, hist
+
+
+def moe_permute(ids, E, x=None):
+    """Stable expert-grouped permutation of ids [T, k]; with x, also the
+    gathered x_sorted [T*k, D]."""
+    T, k = ids.shape
+    _need(ids, "ids", torch.int32, (T, k))
+    D = x.shape[1] if x is not None else 64
+    if x is not None:
+        _need(x, "x", torch.bfloat16, (T, D))
+    d = N.dims(T, D, 64, E, k)
+    dev = ids.device
+    S = T * k
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(S, dtype=torch.int32, device=dev)
+    inv = torch.empty(S, dtype=torch.int32, device=dev)
+    xs = torch.empty(S, D, dtype=torch.bfloat16, device=dev) if x is not None else None
+    nscratch = max(int(lib.moe_permute_scratch_size(d)), 16)
+    scratch = torch.empty(nscratch, dtype=torch.uint8, device=dev)
+    st = lib.moe_permute(_ptr(ids), d, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(x),
+                         _ptr(xs), _ptr(scratch), nscratch, _stream())
+    check(st, "moe_permute")
+    return dict(counts=counts, offsets=offsets, perm=perm, inv=inv, x_sorted=xs)
+
+
+def moe_grouped_swiglu(x_sorted, offsets, W1, W3, T, k, x=None, Ws1=None, Ws3=None, h=None):
+    """h [T*k (+T), F] = silu(A W1[e]) * (A W3[e]) per expert group (+ shared rows)."""
+    S, D = x_sorted.shape
+    E, _, F = W1.shape
+    shared = Ws1 is not None
+    _need(x_sorted, "x_sorted", torch.bfloat16, (T * k, D))
+    _need(W1, "W1", torch.bfloat16, (E, D, F))
+    _need(W3, "W3", torch.bfloat16, (E, D, F))
+    _need(offsets, "offsets", torch.int32, (E + 1,))
+    if shared:
+        _need(x, "x", torch.bfloat16, (T, D))
+        _need(Ws1, "Ws1", torch.bfloat16, (D, F))
+        _need(Ws3, "Ws3", torch.bfloat16, (D, F))
+    rows = T * k + (T if shared else 0)
+    if h is None:
+        h = torch.empty(rows, F, dtype=torch.bfloat16, device=x_sorted.device)
+    st = lib.moe_grouped_swiglu(_ptr(x_sorted), _ptr(x), _ptr(W1), _ptr(W3), _ptr(Ws1), _ptr(Ws3),
+                                _ptr(offsets), N.dims(T, D, F, E, k), _ptr(h), _stream())
+    check(st, "moe_grouped_swiglu")
+    return h
+
+
+def moe_grouped_down(h, offsets, W2, T, k, Ws2=None, y=None):
+    """y [T*k (+T), D] = h W2[e] per expert group (+ shared rows with Ws2)."""
+    E, F, D = W2.shape
+    shared = Ws2 is not None
+    rows = T * k + (T if shared else 0)
+    _need(h, "h", torch.bfloat16, (rows, F))
+    _need(W2, "W2", torch.bfloat16, (E, F, D))
+    _need(Ws2, "Ws2", torch.bfloat16, (F, D))
+    _need(offsets, "offsets", torch.int32, (E + 1,))
+    if y is None:
+        y = torch.empty(rows, D, dtype=torch.bfloat16, device=h.device)
+    st = lib.moe_grouped_down(_ptr(h), _ptr(W2), _ptr(Ws2), _ptr(offsets), N.dims(T, D, F, E, k),
+                              _ptr(y), _stream())
+    check(st, "moe_grouped_down")
+    return y
+
+
+def moe_combine(y, weights, inv, has_shared, out=None):
+    """out[t] = sum_j weights[t, j] * y[inv[t*k + j]] (+ y[T*k + t])."""
+    T, k = weights.shape
+    D = y.shape[1]
+    _need(y, "y", torch.bfloat16)
+    _need(weights, "weights", torch.float32, (T, k))
+    _need(inv, "inv", torch.int32, (T * k,))
+    if out is None:
+        out = torch.empty(T, D, dtype=torch.bfloat16, device=y.device)
+    E = max(k, 1)
+    st = lib.moe_combine(_ptr(y), _ptr(weights), _ptr(inv), N.dims(T, D, 64, E, k), int(bool(has_shared)),
+                         _ptr(out), _stream())
+    check(st, "moe_combine")
+    return out
+
+
+def device_error() -> int:
+    return int(lib.moe_device_error())
+
+
+def launch_count() -> int:
+    return int(lib.moe_launch_count())

@@ -1,0 +1,183 @@
+/*
+ * moe_ffn.h -- C ABI of the GB300 (sm_103a) mixture-of-experts SwiGLU FFN
+ * forward pass.
+ *
+ * The layer (per token t of x [T, D]):
+ *   logits = x[t] . Wg (+ router_bias)                 router GEMM
+ *   ids[t, 0..k-1] = the k largest logits, descending,  top-k
+ *                    equal logits -> lower expert index
+ *   w[t, j] = softmax over the k selected logits        gate weights
+ *   slots s = t*k + j are sorted stably by expert id    permutation
+ *   h = silu(x W1[e]) * (x W3[e])  per routed slot      grouped GEMM W1||W3
+ *   y = h W2[e]                                         grouped GEMM W2
+ *   out[t] = sum_j w[t, j] * y[t, j]  (+ shared(x[t]))  weighted combine
+ * Sources: "Chinchilla scaling, MoE, and fused Triton kernels", section
+ * "PyTorch MoE implementation" (router, top-k, softmax over the selected
+ * logits, stable argsort, bincount, grouped GEMMs, inverse permutation,
+ * weighted sum); "Triton MoE Kernels & Memory Checkpointing", Part A,
+ * section 2 (SwiGLU expert W2(silu(W1 x) * W3 x), top-2 of 8 routed experts
+ * plus an always-on shared expert) and section 10.3 (sort-by-expert layout,
+ * per-expert counts and offsets).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *_host are host memory; every other pointer is device
+ *    memory on the current CUDA device.  The caller owns all memory and the
+ *    stream; the library never allocates, frees or synchronises (except
+ *    moe_device_error, which reads one word back).
+ *  - Tensors are contiguous and row-major.  bf16 tensors are passed as
+ *    void*.  Every device pointer must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *    only enqueued; results are ready when the stream reaches that point.
+ *  - Arguments are validated on the host before anything is enqueued.  A
+ *    bad argument returns MOE_ERR_INVALID_ARG, a shape outside the limits
+ *    below returns MOE_ERR_UNSUPPORTED_SHAPE; nothing is launched in either
+ *    case.  A failed launch returns MOE_ERR_CUDA.  There is no fallback path.
+ *  - Kernels that wait on on-chip barriers give up after a bounded time and
+ *    record MOE_ERR_DEVICE_TIMEOUT in a device word, read by
+ *    moe_device_error().
+ *
+ * Shape limits: 0 <= T <= 2^24; D and F multiples of 64 in [64, 8192]
+ * (the 8192 cap is the page's hard cap on d_model and d_ff);
+ * 1 <= E <= 128; 1 <= k <= min(E, 16).
+ */
+#ifndef MOE_FFN_H
+#define MOE_FFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,
+  MOE_ERR_UNSUPPORTED_SHAPE = -2,
+  MOE_ERR_CUDA = -3,
+  MOE_ERR_WORKSPACE = -4,
+  MOE_ERR_DEVICE_TIMEOUT = -5
+} moe_status;
+
+#define MOE_MAX_EXPERTS 128
+#define MOE_MAX_TOPK 16
+#define MOE_MAX_DIM 8192
+#define MOE_ROUTE_BLOCK_TOKENS 64 /* tokens per router/permute block */
+
+/* Layer dimensions: T tokens, D = d_model, F = d_ff, E routed experts, top-k. */
+typedef struct {
+  int32_t T, D, F, E, k;
+} moe_dims;
+
+/* Optional per-call settings of moe_ffn_forward / moe_ffn_forward_host. */
+typedef struct {
+  /* cudaEvent_t handles recorded on `stream` at the stage boundaries:
+   * [0] before routing, [1] after routing, [2] after the permutation,
+   * [3] after W1||W3, [4] after W2, [5] after the combine.
+   * moe_ffn_forward_host records [6] after the host->device copy of x (before
+   * [0]) and [7] after the device->host copy of out.  NULL entries are skipped. */
+  void* stage_events[8];
+  /* Routing fixed from outside: ids [T, k] int32 and weights [T, k] fp32 in
+   * device memory replace the router when both are non-NULL. */
+  const int32_t* ids_in;
+  const float* weights_in;
+} moe_ffn_options;
+
+/* Bytes of device workspace moe_ffn_forward needs for these dimensions
+ * (has_shared != 0 when the shared expert is used; host_io != 0 adds the
+ * device staging buffers used by moe_ffn_forward_host).  The workspace holds,
+ * each 256-byte aligned: ids [T,k] i32, w [T,k] f32, block histogram
+ * [ceil(T/64), E] i32, counts [E] i32, offsets [E+1] i32, perm [T*k] i32,
+ * inv [T*k] i32, x_sorted [T*k, D] bf16, h [T*k (+T), F] bf16,
+ * y [T*k (+T), D] bf16, then (host_io) x [T, D] and out [T, D] bf16. */
+size_t moe_ffn_workspace_size(moe_dims d, int has_shared, int host_io);
+
+/* Forward pass of one MoE SwiGLU FFN layer.
+ *   x [T, D] bf16; Wg [D, E] bf16; router_bias [E] fp32 or NULL (added to the
+ *   logits in fp32); W1, W3 [E, D, F] bf16; W2 [E, F, D] bf16;
+ *   Ws1, Ws3 [D, F] and Ws2 [F, D] bf16: the shared expert, all three NULL
+ *   for none; out [T, D] bf16.  Router logits and gate weights are fp32, GEMMs
+ *   accumulate in fp32, h and y are stored as bf16, the combine sums in fp32
+ *   and rounds once to bf16.  `workspace` holds moe_ffn_workspace_size(d,
+ *   has_shared, 0) bytes; after the call it contains the routing, the
+ *   permutation and the intermediates in the layout described above.
+ *   opts may be NULL. */
+moe_status moe_ffn_forward(const void* x, const void* Wg, const float* router_bias,
+                           const void* W1, const void* W3, const void* W2,
+                           const void* Ws1, const void* Ws3, const void* Ws2,
+                           moe_dims d, void* out, void* workspace, size_t ws_bytes,
+                           const moe_ffn_options* opts, void* stream);
+
+/* The same forward pass with the activations in host memory: x_host [T, D]
+ * bf16 is copied to the device, the layer runs, and out_host [T, D] bf16 is
+ * copied back, all enqueued on `stream` (use pinned host memory for
+ * asynchronous copies).  Weights stay in device memory.  `workspace` holds
+ * moe_ffn_workspace_size(d, has_shared, 1) bytes. */
+moe_status moe_ffn_forward_host(const void* x_host, const void* Wg, const float* router_bias,
+                                const void* W1, const void* W3, const void* W2,
+                                const void* Ws1, const void* Ws3, const void* Ws2,
+                                moe_dims d, void* out_host, void* workspace, size_t ws_bytes,
+                                const moe_ffn_options* opts, void* stream);
+
+/* ---- Stage entry points (the same kernels moe_ffn_forward launches) ---- */
+
+/* Router GEMM + top-k + softmax ("PyTorch MoE implementation": logits, topk,
+ * softmax over the selected logits).  ids [T, k] int32, weights [T, k] fp32.
+ * block_hist (nullable) receives the per-block expert histogram
+ * [ceil(T/64), E] int32 over tokens [64b, 64b+64). */
+moe_status moe_route(const void* x, const void* Wg, const float* router_bias, moe_dims d,
+                     int32_t* ids, float* weights, int32_t* block_hist, void* stream);
+
+/* Scratch bytes moe_permute needs: the block histogram, ceil(T/64)*E int32. */
+size_t moe_permute_scratch_size(moe_dims d);
+
+/* Stable permutation of the T*k slots by expert id (section "PyTorch MoE
+ * implementation": flatten, stable argsort, bincount; "Triton MoE Kernels",
+ * section 10.3, step 2: gather to expert-sorted order, counts and offsets).
+ *   ids [T, k] int32 in [0, E); counts [E]; offsets [E+1] (offsets[E] = T*k);
+ *   perm [T*k]: sorted position -> slot; inv [T*k]: slot -> sorted position;
+ *   x [T, D] bf16 and x_sorted [T*k, D] bf16 are both NULL or both set
+ *   (x_sorted[p] = x[perm[p] / k]).  Ids outside [0, E) give undefined
+ *   output.  scratch holds moe_permute_scratch_size(d) bytes. */
+moe_status moe_permute(const int32_t* ids, moe_dims d, int32_t* counts, int32_t* offsets,
+                       int32_t* perm, int32_t* inv, const void* x, void* x_sorted,
+                       void* scratch, size_t scratch_bytes, void* stream);
+
+/* Grouped GEMM W1||W3 with the SwiGLU epilogue ("Triton MoE Kernels",
+ * sections 2 and 10.2): for each expert e and sorted row p in
+ * [offsets[e], offsets[e+1]): h[p] = silu(x_sorted[p] W1[e]) * (x_sorted[p] W3[e]).
+ * With the shared expert (Ws1, Ws3 non-NULL, x non-NULL) rows T*k + t of h
+ * receive silu(x[t] Ws1) * (x[t] Ws3).  h holds T*k (+T) rows of F bf16. */
+moe_status moe_grouped_swiglu(const void* x_sorted, const void* x, const void* W1, const void* W3,
+                              const void* Ws1, const void* Ws3, const int32_t* offsets,
+                              moe_dims d, void* h, void* stream);
+
+/* Grouped GEMM W2: y[p] = h[p] W2[e] for the routed rows, and (Ws2 non-NULL)
+ * y[T*k + t] = h[T*k + t] Ws2.  y holds T*k (+T) rows of D bf16. */
+moe_status moe_grouped_down(const void* h, const void* W2, const void* Ws2, const int32_t* offsets,
+                            moe_dims d, void* y, void* stream);
+
+/* Weighted combine ("PyTorch MoE implementation": inverse permutation and
+ * weighted sum): out[t] = sum_j weights[t, j] * y[inv[t*k + j]]
+ * (+ y[T*k + t] when has_shared), summed in fp32 in order j = 0..k-1 and then
+ * the shared term, rounded once to bf16. */
+moe_status moe_combine(const void* y, const float* weights, const int32_t* inv, moe_dims d,
+                       int has_shared, void* out, void* stream);
+
+/* ---- Diagnostics ---- */
+
+/* Reads and clears the device error word of the current device (a
+ * synchronous copy).  Returns MOE_OK or MOE_ERR_DEVICE_TIMEOUT. */
+moe_status moe_device_error(void);
+
+/* Number of kernels this library has launched since it was loaded. */
+uint64_t moe_launch_count(void);
+
+/* Static text for a status code. */
+const char* moe_status_str(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_H */

@@ -1,0 +1,101 @@
+"""The C ABI library builds for sm_103a, loads, exports every declared entry
+point, and rejects bad arguments on the host before any launch (these calls
+need no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_ffn.h")
+
+
+@pytest.fixture(scope="module")
+def native():
+    from grouped_gemm_router_gb300 import build
+    build.build()
+    from grouped_gemm_router_gb300 import _native
+    return _native
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:moe_status|size_t|uint64_t|const char\s*\*)\s*(moe_\w+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(native):
+    names = declared_functions()
+    assert len(names) >= 12
+    lib = ctypes.CDLL(native.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in moe_ffn.h but not exported"
+    assert set(names) == set(native._SIGNATURES), "binding signatures and header disagree"
+
+
+def test_status_strings(native):
+    assert native.status_str(0) == "ok"
+    assert "invalid" in native.status_str(-1)
+    assert native.status_str(-99) == "unknown status"
+
+
+FAKE = 0x100000  # a 16-byte aligned address that is never dereferenced
+
+
+def _forward(native, d, ws_bytes=1 << 40, x=FAKE, out=FAKE, shared=(None, None, None), ws=FAKE):
+    p = ctypes.c_void_p
+    return native.lib.moe_ffn_forward(p(x), p(FAKE), None, p(FAKE), p(FAKE), p(FAKE),
+                                      *(p(s) if s else None for s in shared), d, p(out), p(ws),
+                                      ws_bytes, None, None)
+
+
+def test_argument_validation_before_launch(native):
+    N = native
+    good = N.dims(256, 128, 256, 4, 2)
+    assert _forward(N, N.dims(0, 128, 256, 4, 2)) == N.MOE_OK           # T = 0: nothing to do
+    assert _forward(N, good, x=0) == N.MOE_ERR_INVALID_ARG                # null input
+    assert _forward(N, good, out=FAKE + 4) == N.MOE_ERR_INVALID_ARG       # misaligned
+    assert _forward(N, N.dims(256, 128, 256, 4, 5)) == N.MOE_ERR_INVALID_ARG   # k > E
+    assert _forward(N, N.dims(256, 100, 256, 4, 2)) == N.MOE_ERR_UNSUPPORTED_SHAPE  # D % 64
+    assert _forward(N, N.dims(256, 128, 16384, 4, 2)) == N.MOE_ERR_UNSUPPORTED_SHAPE  # F cap
+    assert _forward(N, N.dims(256, 128, 256, 200, 2)) == N.MOE_ERR_UNSUPPORTED_SHAPE  # E cap
+    assert _forward(N, N.dims(256, 128, 256, 64, 17)) == N.MOE_ERR_UNSUPPORTED_SHAPE  # k cap
+    assert _forward(N, good, shared=(FAKE, None, FAKE)) == N.MOE_ERR_INVALID_ARG   # partial shared
+    assert _forward(N, good, ws_bytes=100) == N.MOE_ERR_WORKSPACE
+    p = ctypes.c_void_p
+    assert N.lib.moe_route(None, p(FAKE), None, good, p(FAKE), p(FAKE), None, None) == N.MOE_ERR_INVALID_ARG
+    assert N.lib.moe_permute(p(FAKE), good, p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), None,
+                             p(FAKE), 1 << 20, None) == N.MOE_ERR_INVALID_ARG   # x without x_sorted
+    assert N.lib.moe_permute(p(FAKE), good, p(FAKE), p(FAKE), p(FAKE), p(FAKE), None, None,
+                             p(FAKE), 4, None) == N.MOE_ERR_WORKSPACE
+    assert N.lib.moe_grouped_swiglu(p(FAKE), None, p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), good,
+                                    p(FAKE), None) == N.MOE_ERR_INVALID_ARG     # shared needs x
+    assert N.lib.moe_combine(p(FAKE), p(FAKE), p(FAKE), N.dims(4, 96, 64, 4, 2), 0, p(FAKE),
+                             None) == N.MOE_ERR_UNSUPPORTED_SHAPE
+    assert N.lib.moe_launch_count() == 0
+
+
+def test_workspace_size_matches_documented_layout(native):
+    def layout(T, D, F, E, k, shared, host_io):
+        a = lambda n: (n + 255) // 256 * 256
+        S = T * k
+        rows = S + (T if shared else 0)
+        nblk = (T + 63) // 64
+        n = a(S * 4) * 2 + a(nblk * E * 4) + a(E * 4) + a((E + 1) * 4) + a(S * 4) * 2
+        n += a(S * D * 2) + a(rows * F * 2) + a(rows * D * 2)
+        if host_io:
+            n += 2 * a(T * D * 2)
+        return n
+
+    for T, D, F, E, k, sh, hio in [(256, 128, 256, 4, 2, 0, 0), (32768, 768, 1536, 8, 2, 1, 1),
+                                   (2048, 768, 1536, 64, 4, 1, 0), (1, 64, 64, 1, 1, 0, 1)]:
+        assert native.lib.moe_ffn_workspace_size(native.dims(T, D, F, E, k), sh, hio) == \
+            layout(T, D, F, E, k, sh, hio)
+    assert native.lib.moe_ffn_workspace_size(native.dims(10, 100, 64, 4, 2), 0, 0) == 0
+
+
+def test_product_path_fails_loudly_without_library(tmp_path):
+    from grouped_gemm_router_gb300 import _native
+    with pytest.raises(ImportError):
+        _native.load(str(tmp_path / "missing.so"))

@@ -1,0 +1,225 @@
+"""Stage-by-stage parity of the CUDA path (through the C ABI) with the fp64
+oracle: routing, permutation (bit-exact), the two grouped GEMMs and the
+combine, on small multi-tile shapes with ragged groups, empty experts and the
+degenerate cases, and on the full-size workloads."""
+import numpy as np
+import pytest
+import torch
+
+from grouped_gemm_router_gb300 import inputs
+from oracle import moe_oracle as orc
+
+from _util import assert_close, bf16_bits, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+# Intermediates h and y are rounded once to bf16 after fp32 accumulation of
+# exact bf16 products: |err| <= 2^-9 |ref| plus fp32 summation noise.
+H_RTOL, H_ATOL = 4e-3, 1e-4
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from grouped_gemm_router_gb300 import build
+    build.build()
+    from grouped_gemm_router_gb300 import moe as m
+    return m
+
+
+def _layer(T, D, F, E, k, shared, seed, bias=None):
+    return inputs.make_custom(T, D, F, E, k, shared, seed, bias=bias)
+
+
+def _oracle_routing(L, k):
+    x, Wg = orc.bf16_to_f64(L["x"]), orc.bf16_to_f64(L["Wg"])
+    logits = orc.router_logits(x, Wg, L["bias"])
+    ids, w = orc.topk_softmax(logits, k)
+    return logits, ids, w, orc.topk_gap(logits, k)
+
+
+ROUTE_CASES = [
+    # T, D, F, E, k, shared, seed, bias
+    (256, 128, 256, 4, 2, False, 0, None),
+    (1000, 256, 64, 8, 2, False, 1, None),
+    (1, 64, 64, 3, 1, False, 2, None),
+    (333, 192, 64, 20, 5, False, 3, None),          # E padded to 24
+    (300, 512, 64, 64, 4, False, 4, None),
+    (200, 384, 64, 128, 16, False, 5, None),        # widest router, largest k
+    (257, 4608, 64, 8, 2, False, 6, None),          # D larger than one staged chunk for E=8? no; long D
+    (500, 768, 64, 8, 2, False, 7, inputs.zipf_router_bias(8, 1.2, 7)),
+]
+
+
+@pytest.mark.parametrize("case", ROUTE_CASES, ids=lambda c: f"T{c[0]}_D{c[1]}_E{c[3]}_k{c[4]}")
+def test_route(moe, case):
+    T, D, F, E, k, shared, seed, bias = case
+    w_, L = _layer(T, D, F, E, k, shared, seed, bias)
+    logits, ids_ref, w_ref, gap = _oracle_routing(L, k)
+    ids, w, hist = moe.moe_route(to_dev(L["x"]), to_dev(L["Wg"]), k,
+                                 bias=to_dev(L["bias"]) if L["bias"] is not None else None)
+    torch.cuda.synchronize()
+    ids, w, hist = ids.cpu().numpy(), w.cpu().numpy(), hist.cpu().numpy()
+    near = gap < 1e-3
+    mism = (ids != ids_ref).any(axis=1)
+    assert not (mism & ~near).any(), f"{int((mism & ~near).sum())} tokens differ outside the near-tie window"
+    ok = ~mism
+    assert np.abs(w[ok] - w_ref[ok]).max() < 1e-4
+    assert np.abs(w.sum(axis=1) - 1).max() < 1e-5
+    for b in range(hist.shape[0]):  # per-64-token-block histogram of the GPU's own ids
+        blk = ids[b * 64:(b + 1) * 64].reshape(-1)
+        assert (hist[b] == np.bincount(blk, minlength=E)).all()
+
+
+def test_route_all_ties_pick_lowest_experts(moe):
+    T, D, E, k = 130, 128, 8, 3
+    x = to_dev(inputs.f32_to_bf16_bits(np.random.default_rng(0).normal(size=(T, D)).astype(np.float32)))
+    Wg = torch.zeros(D, E, dtype=torch.bfloat16, device="cuda")
+    ids, w, _ = moe.moe_route(x, Wg, k)
+    assert (ids.cpu().numpy() == np.arange(k)).all()
+    assert (w.cpu().numpy() == np.float32(1.0 / 3.0)).all()
+
+
+PERM_CASES = [
+    # T, E, k, distribution
+    (1, 1, 1, "uniform"), (63, 8, 2, "uniform"), (64, 8, 2, "uniform"), (65, 8, 2, "uniform"),
+    (1000, 8, 2, "uniform"), (300, 128, 16, "uniform"), (777, 5, 3, "one_expert_heavy"),
+    (4096, 16, 2, "zipf_with_empty"), (32768, 8, 2, "uniform"), (2048, 64, 4, "uniform"),
+]
+
+
+def _ids(T, E, k, dist, seed):
+    rng = np.random.default_rng(seed)
+    if dist == "uniform":
+        return np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    if dist == "one_expert_heavy":
+        out = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+        out[:, 0] = 2
+        out[:, 1:] = np.where(out[:, 1:] == 2, 4, out[:, 1:])
+        return out.astype(np.int32)
+    p = np.array([(e + 1) ** -1.2 for e in range(E)])
+    p[E - 1] = 0
+    p /= p.sum()
+    return np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("case", PERM_CASES, ids=lambda c: f"T{c[0]}_E{c[1]}_k{c[2]}_{c[3]}")
+def test_permute_bit_exact(moe, case):
+    T, E, k, dist = case
+    ids = _ids(T, E, k, dist, T + E)
+    D = 128
+    x = inputs.f32_to_bf16_bits(np.random.default_rng(T).normal(size=(T, D)).astype(np.float32))
+    r = moe.moe_permute(to_dev(ids), E, x=to_dev(x))
+    torch.cuda.synchronize()
+    ref = orc.permutation(ids, E)
+    for key in ("counts", "offsets", "perm", "inv"):
+        got = r[key].cpu().numpy()
+        assert (got == ref[key]).all(), f"{key} differs"
+    xs = bf16_bits(r["x_sorted"])
+    assert (xs == x[ref["perm"] // k]).all()
+
+
+def _grouped_inputs(L, k, E):
+    _, ids, w, _ = _oracle_routing(L, k)
+    pm = orc.permutation(ids, E)
+    xs_bits = L["x"][pm["perm"].astype(np.int64) // k]
+    return ids, w, pm, xs_bits
+
+
+GEMM_CASES = [
+    # T, D, F, E, k, shared, seed, bias
+    (256, 128, 256, 4, 2, False, 10, None),
+    (256, 128, 256, 4, 2, True, 11, None),
+    (300, 192, 192, 5, 2, True, 12, None),            # 64-wide tiles on both GEMMs
+    (1000, 384, 640, 16, 3, False, 13, np.array([0, -1e4, 0, 0, 0, -1e4, 0, 0, 0, 0, 0, 0, 0, 0, 0, -1e4], np.float32)),
+    (512, 256, 256, 128, 4, True, 14, None),           # 128 tiny groups
+    (1, 64, 64, 2, 2, True, 15, None),                # S = 2 rows, smaller than one tile
+    (700, 128, 128, 8, 2, False, 16, np.array([60, 50, 0, 0, 0, 0, 0, 0], np.float32)),  # two hot experts
+    (2048, 768, 1536, 64, 4, True, 3, None),          # small-chunk shape
+    (640, 2048, 1024, 4, 1, False, 17, None),         # long K (32 k-blocks)
+]
+
+
+@pytest.mark.parametrize("case", GEMM_CASES, ids=lambda c: f"T{c[0]}_D{c[1]}_F{c[2]}_E{c[3]}_k{c[4]}_sh{int(c[5])}")
+def test_grouped_gemms(moe, case):
+    T, D, F, E, k, shared, seed, bias = case
+    w_, L = _layer(T, D, F, E, k, shared, seed, bias)
+    ids, w, pm, xs_bits = _grouped_inputs(L, k, E)
+    offs = to_dev(pm["offsets"])
+    h = moe.moe_grouped_swiglu(to_dev(xs_bits), offs, to_dev(L["W1"]), to_dev(L["W3"]), T, k,
+                               x=to_dev(L["x"]) if shared else None,
+                               Ws1=to_dev(L["Ws1"]), Ws3=to_dev(L["Ws3"]))
+    torch.cuda.synchronize()
+    S = T * k
+    h_ref = orc.grouped_swiglu(orc.bf16_to_f64(xs_bits), orc.bf16_to_f64(L["W1"]),
+                               orc.bf16_to_f64(L["W3"]), pm["offsets"])
+    h_got = to_f64(h)
+    assert_close(h_got[:S], h_ref, "h (routed)", atol=H_ATOL, rtol=H_RTOL)
+    if shared:
+        x64 = orc.bf16_to_f64(L["x"])
+        hs_ref = orc.silu(x64 @ orc.bf16_to_f64(L["Ws1"])) * (x64 @ orc.bf16_to_f64(L["Ws3"]))
+        assert_close(h_got[S:], hs_ref, "h (shared)", atol=H_ATOL, rtol=H_RTOL)
+    # down projection on the GPU's own (bf16) h
+    y = moe.moe_grouped_down(h, offs, to_dev(L["W2"]), T, k, Ws2=to_dev(L["Ws2"]))
+    torch.cuda.synchronize()
+    y_ref = orc.grouped_down(h_got[:S], orc.bf16_to_f64(L["W2"]), pm["offsets"])
+    y_got = to_f64(y)
+    assert_close(y_got[:S], y_ref, "y (routed)", atol=H_ATOL, rtol=H_RTOL)
+    if shared:
+        assert_close(y_got[S:], h_got[S:] @ orc.bf16_to_f64(L["Ws2"]), "y (shared)", atol=H_ATOL, rtol=H_RTOL)
+    # combine on the GPU's own y
+    out = moe.moe_combine(y, to_dev(w.astype(np.float32)), to_dev(pm["inv"]), shared)
+    torch.cuda.synchronize()
+    out_ref = orc.combine(y_got[:S], pm["inv"], w.astype(np.float32).astype(np.float64),
+                          y_got[S:] if shared else None)
+    assert_close(to_f64(out), out_ref, "combine", atol=1e-3, rtol=4e-3)
+    assert moe.device_error() == 0
+
+
+def test_combine_exact_small(moe):
+    """Combine with y values and weights that are exact in bf16/fp32: the
+    fp32 sum is exact, so the bf16 output equals the rounded fp64 sum."""
+    T, D, k = 70, 64, 3
+    rng = np.random.default_rng(1)
+    S = T * k
+    y = (rng.integers(-64, 64, size=(S + T, D)) / 16.0).astype(np.float32)
+    perm = rng.permutation(S).astype(np.int32)
+    inv = np.empty(S, np.int32)
+    inv[perm] = np.arange(S, dtype=np.int32)
+    w = (rng.integers(1, 8, size=(T, k)) / 8.0).astype(np.float32)
+    out = moe.moe_combine(to_dev(inputs.f32_to_bf16_bits(y)), to_dev(w), to_dev(inv), True)
+    ref = orc.combine(y[:S].astype(np.float64), inv, w.astype(np.float64), y[S:].astype(np.float64))
+    assert (bf16_bits(out) == inputs.f32_to_bf16_bits(ref.astype(np.float32))).all()
+
+
+@pytest.mark.parametrize("name", ["gptoss_lite", "wide"])
+def test_grouped_gemms_full_size_sampled(moe, name):
+    """Full-size grouped GEMMs (the launch configuration of the benchmark),
+    checked on sampled rows that the oracle computes one expert at a time."""
+    w_ = inputs.WORKLOADS[name]
+    L = inputs.make_layer(w_)
+    T, D, F, E, k = w_.T, w_.D, w_.F, w_.E, w_.k
+    ids, w, pm, xs_bits = _grouped_inputs(L, k, E)
+    offs = to_dev(pm["offsets"])
+    h = moe.moe_grouped_swiglu(to_dev(xs_bits), offs, to_dev(L["W1"]), to_dev(L["W3"]), T, k,
+                               x=to_dev(L["x"]) if w_.shared else None,
+                               Ws1=to_dev(L["Ws1"]), Ws3=to_dev(L["Ws3"]))
+    y = moe.moe_grouped_down(h, offs, to_dev(L["W2"]), T, k, Ws2=to_dev(L["Ws2"]))
+    torch.cuda.synchronize()
+    S = T * k
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(S, size=256, replace=False))
+    # include every group boundary row and the last row
+    rows = np.unique(np.concatenate([rows, pm["offsets"][1:-1], pm["offsets"][1:-1] - 1, [S - 1]]))
+    rows = rows[(rows >= 0) & (rows < S)]
+    expert = np.searchsorted(pm["offsets"], rows, side="right") - 1
+    h_got = to_f64(h[torch.from_numpy(rows).cuda()])
+    y_got = to_f64(y[torch.from_numpy(rows).cuda()])
+    for e in np.unique(expert):
+        sel = expert == e
+        xs = orc.bf16_to_f64(xs_bits[rows[sel]])
+        one = np.array([0, int(sel.sum())])
+        h_ref = orc.grouped_swiglu(xs, orc.bf16_to_f64(L["W1"][e:e + 1]), orc.bf16_to_f64(L["W3"][e:e + 1]), one)
+        assert_close(h_got[sel], h_ref, f"h expert {e}", atol=H_ATOL, rtol=H_RTOL)
+        y_ref = orc.grouped_down(h_got[sel], orc.bf16_to_f64(L["W2"][e:e + 1]), one)
+        assert_close(y_got[sel], y_ref, f"y expert {e}", atol=H_ATOL, rtol=H_RTOL)
+    assert moe.device_error() == 0
