@@ -164,6 +164,25 @@ moe_status moe_grouped_down(const void* h, const void* W2, const void* Ws2, cons
 moe_status moe_combine(const void* y, const float* weights, const int32_t* inv, moe_dims d,
                        int has_shared, void* out, void* stream);
 
+/* ---- Allocation-free variant ---- */
+
+/* moe_permute without a caller-provided scratch buffer, for callers that
+ * cannot allocate device memory (for example a plugin inside a host framework
+ * that owns all device memory, or a path that must never call cudaMalloc).
+ * The pages have no counterpart of this entry point; it exists for such
+ * callers only.  Arguments and results are those of moe_permute.  The block
+ * histogram lives in a fixed 65,536-entry int32 array (256 KB) in the
+ * library's own device memory, held on every GPU that loads the library until
+ * the process exits; calls with ceil(T/64) * E > 65,536 return
+ * MOE_ERR_UNSUPPORTED_SHAPE.  Every call shares that array: calls whose work
+ * overlaps on the GPU race and must be serialised by the caller.  The first
+ * call on each device looks up the array's device address (with that device
+ * current); make it before any stream capture.  It calls no cudaMalloc or
+ * cudaFree. */
+moe_status moe_permute_noalloc(const int32_t* ids, moe_dims d, int32_t* counts, int32_t* offsets,
+                               int32_t* perm, int32_t* inv, const void* x, void* x_sorted,
+                               void* stream);
+
 /* ---- Diagnostics ---- */
 
 /* Reads and clears the device error word of the current device (a
