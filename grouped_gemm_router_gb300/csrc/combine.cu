@@ -18,6 +18,19 @@ namespace moe {
 constexpr int kCombineThreads = 256;
 constexpr int kCombineWarps = kCombineThreads / 32;
 
+MOE_DEV void fma_bf16x8(float (&acc)[8], float w, const uint4& v) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    acc[2 * q] = fmaf(w, bf16_lo(u[q]), acc[2 * q]);
+    acc[2 * q + 1] = fmaf(w, bf16_hi(u[q]), acc[2 * q + 1]);
+  }
+}
+
+// One warp per token.  KMAX >= k is a compile-time bound so the k row
+// pointers and weights stay in registers; each lane loads all k (+1) rows of
+// U 16-byte column chunks before doing any arithmetic.
+template <int KMAX, int U>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const uint4* __restrict__ y, const float* __restrict__ w, const int32_t* __restrict__ inv, int T,
     int D, int k, int S, int has_shared, uint4* __restrict__ out) {
@@ -25,65 +38,82 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
   const int t = blockIdx.x * kCombineWarps + warp;
   if (t >= T) return;
   const int n16 = D >> 3;
-  // lane j < k fetches slot t*k + j; broadcast below
   int my_row = 0;
   float my_w = 0.f;
   if (lane < k) {
     my_row = inv[static_cast<size_t>(t) * k + lane];
     my_w = w[static_cast<size_t>(t) * k + lane];
   }
-  int rows[MOE_MAX_TOPK];
-  float ws[MOE_MAX_TOPK];
+  const uint4* rows[KMAX];
+  float ws[KMAX];
 #pragma unroll
-  for (int j = 0; j < MOE_MAX_TOPK; ++j) {
-    rows[j] = __shfl_sync(0xffffffffu, my_row, j);
+  for (int j = 0; j < KMAX; ++j) {
+    rows[j] = y + static_cast<size_t>(__shfl_sync(0xffffffffu, my_row, j)) * n16;
     ws[j] = __shfl_sync(0xffffffffu, my_w, j);
   }
   const uint4* ysh = y + static_cast<size_t>(S + t) * n16;
-  for (int c = lane; c < n16; c += 32) {
-    uint4 v[MOE_MAX_TOPK];
+  uint4* orow = out + static_cast<size_t>(t) * n16;
+  for (int c0 = lane; c0 < n16; c0 += 32 * U) {
+    uint4 v[U][KMAX];
+    uint4 vs[U];
 #pragma unroll
-    for (int j = 0; j < MOE_MAX_TOPK; ++j)
-      if (j < k) v[j] = __ldg(y + static_cast<size_t>(rows[j]) * n16 + c);
-    uint4 vs = make_uint4(0, 0, 0, 0);
-    if (has_shared) vs = __ldg(ysh + c);
-    float acc[8];
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + 32 * u;
+      const bool in = c < n16;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      for (int j = 0; j < KMAX; ++j)
+        if (j < k && in) v[u][j] = __ldg(rows[j] + c);
+      vs[u] = (has_shared && in) ? __ldg(ysh + c) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-    for (int j = 0; j < MOE_MAX_TOPK; ++j) {
-      if (j < k) {
-        const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + 32 * u;
+      if (c >= n16) break;
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (j < k) fma_bf16x8(acc, ws[j], v[u][j]);
+      if (has_shared) {
+        const uint32_t q4[4] = {vs[u].x, vs[u].y, vs[u].z, vs[u].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          acc[2 * q] = fmaf(ws[j], bf16_lo(u[q]), acc[2 * q]);
-          acc[2 * q + 1] = fmaf(ws[j], bf16_hi(u[q]), acc[2 * q + 1]);
+          acc[2 * q] += bf16_lo(q4[q]);
+          acc[2 * q + 1] += bf16_hi(q4[q]);
         }
       }
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      orow[c] = o;
     }
-    if (has_shared) {
-      const uint32_t u[4] = {vs.x, vs.y, vs.z, vs.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc[2 * q] += bf16_lo(u[q]);
-        acc[2 * q + 1] += bf16_hi(u[q]);
-      }
-    }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    out[static_cast<size_t>(t) * n16 + c] = o;
   }
+}
+
+template <int KMAX, int U>
+static void launch_combine_k(const uint16_t* y, const float* w, const int32_t* inv, const moe_dims& d,
+                             int has_shared, uint16_t* out, cudaStream_t s) {
+  const int grid = (d.T + kCombineWarps - 1) / kCombineWarps;
+  combine_kernel<KMAX, U><<<grid, kCombineThreads, 0, s>>>(
+      reinterpret_cast<const uint4*>(y), w, inv, d.T, d.D, d.k, d.T * d.k, has_shared,
+      reinterpret_cast<uint4*>(out));
 }
 
 cudaError_t launch_combine(const uint16_t* y, const float* w, const int32_t* inv, const moe_dims& d,
                            int has_shared, uint16_t* out, cudaStream_t s) {
-  const int grid = (d.T + kCombineWarps - 1) / kCombineWarps;
-  combine_kernel<<<grid, kCombineThreads, 0, s>>>(reinterpret_cast<const uint4*>(y), w, inv, d.T, d.D,
-                                                  d.k, d.T * d.k, has_shared,
-                                                  reinterpret_cast<uint4*>(out));
+  if (d.k <= 1)
+    launch_combine_k<1, 4>(y, w, inv, d, has_shared, out, s);
+  else if (d.k <= 2)
+    launch_combine_k<2, 3>(y, w, inv, d, has_shared, out, s);
+  else if (d.k <= 4)
+    launch_combine_k<4, 2>(y, w, inv, d, has_shared, out, s);
+  else if (d.k <= 8)
+    launch_combine_k<8, 1>(y, w, inv, d, has_shared, out, s);
+  else
+    launch_combine_k<16, 1>(y, w, inv, d, has_shared, out, s);
   note_launch();
   return cudaGetLastError();
 }

@@ -22,10 +22,11 @@
 // the device from the offsets (no host synchronisation): tiles are numbered
 // group by group, n fastest, and CTA b takes tiles b, b + grid, ...
 //
-// Warp roles (192 threads, one CTA per SM):
+// Warp roles (320 threads, one CTA per SM):
 //   warp 0     TMA producer (one lane)
 //   warp 1     TMEM allocator + MMA issuer (one lane)
-//   warps 2-5  epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31
+//   warps 2-9  epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 and the
+//              columns of half (w - 2) / 4 of the tile
 // Pipelines: kStages shared-memory stages (full / empty mbarriers) and two
 // TMEM accumulators of 256 columns (tmem_full / tmem_empty), so the epilogue
 // of one tile overlaps the MMAs of the next.
@@ -53,7 +54,8 @@ constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;        // 16 KB
 constexpr int kBBytesMax = 256 * kBK * 2;     // 32 KB
 constexpr int kStageBytes = kABytes + kBBytesMax;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
 constexpr int kMaxGroups = MOE_MAX_EXPERTS + 1;
 constexpr uint32_t kTmemCols = 512;           // two 256-column accumulators
 constexpr int kSmemBytes = kStages * kStageBytes + 1024;
@@ -150,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int b = 0; b < 2; ++b) {
         mbar_init(smem_u32(&ctl.tfull[b]), 1);
-        mbar_init(smem_u32(&ctl.tempty[b]), 4);
+        mbar_init(smem_u32(&ctl.tempty[b]), kEpiWarps);
       }
       mbar_init(smem_u32(&ctl.drain), 1);
       ctl.abort = 0;
@@ -283,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ===================== epilogue =====================
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // which half of the tile's columns
     const int r_in_tile = q * 32 + lane;
     int g = 0;
     int i = 0;
@@ -299,8 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = row < ctl.nrows[g];
       uint16_t* crow = p.C + static_cast<size_t>(ctl.row0[g] + (valid ? row : 0)) * p.N + n * hw;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * 256;
+      const int c_lo = half * (hw / 2), c_hi = c_lo + hw / 2;
       if (kSwiGLU) {
-        for (int cc = 0; cc < hw; cc += 32) {
+        for (int cc = c_lo; cc < c_hi; cc += 32) {
           uint32_t rg[32], ru[32];
           tmem_ld_32cols(taddr + cc, rg);
           tmem_ld_32cols(taddr + hw + cc, ru);
@@ -310,8 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) {
             const float g0 = __uint_as_float(rg[2 * j]), g1 = __uint_as_float(rg[2 * j + 1]);
             const float u0 = __uint_as_float(ru[2 * j]), u1 = __uint_as_float(ru[2 * j + 1]);
-            const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
-            const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+            // silu(g) = g / (1 + exp(-g)); the fast division returns 0 when
+            // exp(-g) overflows, which is the limit of silu for g -> -inf.
+            const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+            const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
             packed[j] = pack_bf16x2(h0, h1);
           }
           if (valid) {
@@ -322,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        for (int cc = 0; cc < hw; cc += 32) {
+        for (int cc = c_lo; cc < c_hi; cc += 32) {
           uint32_t ra[32];
           tmem_ld_32cols(taddr + cc, ra);
           tmem_ld_wait();

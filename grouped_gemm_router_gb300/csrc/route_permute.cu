@@ -66,29 +66,67 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(
 #pragma unroll
   for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 
-  constexpr int EP = NT * 8;  // experts padded to whole MMA tiles
+  constexpr int EP = NT * 8;              // experts padded to whole MMA tiles
+  constexpr int KG = (NT >= 8) ? 4 : 8;   // 32-wide chunks loaded per batch
   for (int d0 = 0; d0 < D; d0 += dchunk) {
     const int dc = min(dchunk, D - d0);
     __syncthreads();
-    for (int i = threadIdx.x; i < dc * EP; i += blockDim.x) {
-      const int dd = i / EP, e = i - dd * EP;
-      const uint16_t v = (e < E) ? Wg[static_cast<size_t>(d0 + dd) * E + e] : uint16_t(0);
-      const int kc = dd >> 5, r = dd & 31;
-      const int ln = (e & 7) * 4 + (r >> 3);
-      wpack16[((static_cast<size_t>(kc) * NT + (e >> 3)) * 32 + ln) * 8 + (r & 7)] = v;
+    // Stage Wg[d0 : d0 + dc, :] (dc * E contiguous bf16, a multiple of 8) in
+    // fragment order, 16-byte loads issued in batches; padded experts are 0.
+    if (E < EP) {
+      const int nz = dc * EP / 8;
+      for (int i = threadIdx.x; i < nz; i += blockDim.x) wpack[i] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(Wg + static_cast<size_t>(d0) * E);
+    const int nvec = dc * E / 8;
+    for (int base = threadIdx.x; base < nvec; base += blockDim.x * 4) {
+      uint4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int idx = base + j * blockDim.x;
+        v[j] = idx < nvec ? __ldg(src + idx) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int idx = base + j * blockDim.x;
+        if (idx >= nvec) continue;
+        const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        int dd = (idx * 8) / E, e = idx * 8 - dd * E;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const uint16_t val = static_cast<uint16_t>((t & 1) ? (w4[t >> 1] >> 16) : (w4[t >> 1] & 0xFFFFu));
+          const int kc = dd >> 5, r = dd & 31;
+          const int ln = (e & 7) * 4 + (r >> 3);
+          wpack16[((static_cast<size_t>(kc) * NT + (e >> 3)) * 32 + ln) * 8 + (r & 7)] = val;
+          if (++e == E) {
+            e = 0;
+            ++dd;
+          }
+        }
+      }
     }
     __syncthreads();
     const int nkc = dc >> 5;
-#pragma unroll 4
-    for (int kc = 0; kc < nkc; ++kc) {
-      const int q = ((d0 + kc * 32) >> 3) + c;  // 16-byte column index
-      const uint4 a0 = ok0 ? __ldg(xr0 + q) : make_uint4(0, 0, 0, 0);
-      const uint4 a1 = ok1 ? __ldg(xr1 + q) : make_uint4(0, 0, 0, 0);
+    for (int kc0 = 0; kc0 < nkc; kc0 += KG) {
+      // all x loads of the batch first (2 rows x KG chunks of 16 bytes)
+      uint4 a0[KG], a1[KG];
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        const uint4 b = wpack[(static_cast<size_t>(kc) * NT + n) * 32 + lane];
-        mma_m16n8k16_bf16(acc[n], a0.x, a1.x, a0.y, a1.y, b.x, b.y);
-        mma_m16n8k16_bf16(acc[n], a0.z, a1.z, a0.w, a1.w, b.z, b.w);
+      for (int j = 0; j < KG; ++j) {
+        const int q = ((d0 + (kc0 + j) * 32) >> 3) + c;  // 16-byte column index
+        const bool in = kc0 + j < nkc;
+        a0[j] = (ok0 && in) ? __ldg(xr0 + q) : make_uint4(0, 0, 0, 0);
+        a1[j] = (ok1 && in) ? __ldg(xr1 + q) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < KG; ++j) {
+        if (kc0 + j >= nkc) break;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const uint4 b = wpack[(static_cast<size_t>(kc0 + j) * NT + n) * 32 + lane];
+          mma_m16n8k16_bf16(acc[n], a0[j].x, a1[j].x, a0[j].y, a1[j].y, b.x, b.y);
+          mma_m16n8k16_bf16(acc[n], a0[j].z, a1[j].z, a0[j].w, a1[j].w, b.z, b.w);
+        }
       }
     }
   }
@@ -180,7 +218,10 @@ __global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ i
   __syncthreads();
   const int s0 = blockIdx.x * kRouteTokens * k;  // T * k <= 2^28 fits in int
   const int ns = min(kRouteTokens * k, T * k - s0);
-  for (int i = threadIdx.x; i < ns; i += blockDim.x) atomicAdd(&s_hist[ids[s0 + i]], 1);
+  for (int i = threadIdx.x; i < ns; i += blockDim.x) {
+    const int e = ids[s0 + i];
+    if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicAdd(&s_hist[e], 1);
+  }
   __syncthreads();
   for (int i = threadIdx.x; i < E; i += blockDim.x)
     hist[static_cast<size_t>(blockIdx.x) * E + i] = s_hist[i];
@@ -274,13 +315,18 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
     __syncthreads();
     const int li = base + tid;
     const bool valid = li < ns;
-    const int ex = valid ? ids[s0 + li] : -1;
+    int ex = valid ? ids[s0 + li] : -1;
+    if (static_cast<unsigned>(ex) >= static_cast<unsigned>(E)) ex = -1;  // not placed
     const unsigned peers = __match_any_sync(0xffffffffu, ex);
     const unsigned lt = (1u << lane) - 1u;
     const int rank = __popc(peers & lt);
-    if (valid && (__ffs(peers) - 1) == lane) s_wcnt[warp][ex] = __popc(peers);
+    if (ex >= 0 && (__ffs(peers) - 1) == lane) s_wcnt[warp][ex] = __popc(peers);
     __syncthreads();
-    if (valid) {
+    if (valid && ex < 0) {
+      inv[s0 + li] = 0;  // an id outside [0, E): the slot gets no row of its own
+      s_pos[li] = -1;
+    }
+    if (ex >= 0) {
       int pos = s_base[ex] + rank;
       for (int w = 0; w < warp; ++w) pos += s_wcnt[w][ex];
       perm[pos] = s0 + li;
@@ -296,22 +342,37 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
     __syncthreads();
   }
 
-  // ---- 3. gather rows ----
+  // ---- 3. gather rows: each warp copies 4 rows at a time ----
   if (x == nullptr) return;
   const int n16 = D >> 3;  // 16-byte vectors per row
-  for (int i = warp; i < ns; i += kScatterWarps) {
-    const uint4* src = x + static_cast<size_t>((s0 + i) / k) * n16;
-    uint4* dst = xs + static_cast<size_t>(s_pos[i]) * n16;
-    int cidx = lane;
-    for (; cidx + 96 < n16; cidx += 128) {
-      const uint4 v0 = __ldg(src + cidx), v1 = __ldg(src + cidx + 32);
-      const uint4 v2 = __ldg(src + cidx + 64), v3 = __ldg(src + cidx + 96);
-      dst[cidx] = v0;
-      dst[cidx + 32] = v1;
-      dst[cidx + 64] = v2;
-      dst[cidx + 96] = v3;
+  constexpr int RW = 4;
+  for (int i0 = warp * RW; i0 < ns; i0 += kScatterWarps * RW) {
+    const uint4* src[RW];
+    uint4* dst[RW];
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+      const int i = i0 + r;
+      const bool ok = i < ns && s_pos[i] >= 0;
+      src[r] = ok ? x + static_cast<size_t>((s0 + i) / k) * n16 : nullptr;
+      dst[r] = ok ? xs + static_cast<size_t>(s_pos[i]) * n16 : nullptr;
     }
-    for (; cidx < n16; cidx += 32) dst[cidx] = __ldg(src + cidx);
+    for (int c0 = lane; c0 < n16; c0 += 64) {
+      uint4 v[RW][2];
+#pragma unroll
+      for (int r = 0; r < RW; ++r)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int cidx = c0 + 32 * u;
+          if (src[r] != nullptr && cidx < n16) v[r][u] = __ldg(src[r] + cidx);
+        }
+#pragma unroll
+      for (int r = 0; r < RW; ++r)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int cidx = c0 + 32 * u;
+          if (dst[r] != nullptr && cidx < n16) dst[r][cidx] = v[r][u];
+        }
+    }
   }
 }
 
