@@ -145,6 +145,18 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def reduce_max(value: float, device) -> float:
+    """Max of a per-rank value over all ranks (the value itself without a
+    process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def to_dev(a, dev):
     import torch
     if a is None:
@@ -293,11 +305,7 @@ def main():
 
     stage_ms = np.array([[evs[i][s].elapsed_time(evs[i][s + 1]) for s in range(5)] for i in range(K)])
     step_ms = np.array([evs[i][0].elapsed_time(evs[i][5]) for i in range(K)])
-    ms = float(step_ms.mean())
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(float(step_ms.mean()), dev)
 
     # ---- end to end through the host-memory entry point ----
     ws_h = moe.Workspace(T, D, F, E, k, w.shared, host_io=True, device=dev)
@@ -315,11 +323,7 @@ def main():
         torch.cuda.synchronize()
         if i >= args.warmup:
             e2e_ms.append(ev[6].elapsed_time(ev[7]))
-    e2e = float(np.mean(e2e_ms))
-    if world > 1:
-        t = torch.tensor([e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e = float(t.item())
+    e2e = reduce_max(float(np.mean(e2e_ms)), dev)
 
     pk, pk_kind = peaks()
     names = ["route", "permute", "w1w3", "w2", "combine"]
