@@ -333,7 +333,7 @@ def main():
     tokens_s = T * world / (ms / 1e3)
     w1w3_s = st_mean["w1w3"] / 1e3
     achieved = w1w3_flops_per_launch(w) / w1w3_s / 1e12
-    traffic = ncu_traffic("grouped_gemm_kernel<true>")
+    traffic = ncu_traffic("grouped_gemm_pair_kernel<true>")
     hbm_stages = st_mean["route"] + st_mean["permute"] + st_mean["combine"]
     hbm_bytes = sb["route"] + sb["permute"] + sb["combine"]
 
@@ -357,7 +357,7 @@ def main():
         "active_tflops": fl * world / (ms / 1e3) / 1e12,
         "frac_of_bf16_peak": fl / (ms / 1e3) / 1e12 / pk["bf16_tflops"],
         "stage_ms": st_mean,
-        "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel<true> (W1||W3 + SiLU*mul)",
+        "roofline": {"bound": "tensor", "kernel": "grouped_gemm_pair_kernel<true> (W1||W3 + SiLU*mul)",
                      "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
                      "peak_kind": f"{pk_kind} bf16 burst"},

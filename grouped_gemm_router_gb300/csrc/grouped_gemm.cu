@@ -1,5 +1,6 @@
 // Persistent ragged grouped GEMM on the 5th-generation tensor cores
-// (tcgen05.mma, accumulators in TMEM, operands staged by TMA).
+// (tcgen05.mma, accumulators in TMEM, operands staged by TMA), run by CTA
+// pairs (clusters of two CTAs on two SMs, cta_group::2).
 //
 // Two epilogues share one engine:
 //  * SwiGLU (W1||W3): for every sorted row p of expert e,
@@ -9,34 +10,41 @@
 //    and u never leave the chip; the epilogue reads both from TMEM, applies
 //    silu(g) * u in fp32 and stores bf16 h.  This is the fused W1/W3 + SiLU
 //    stage of "Triton MoE Kernels & Memory Checkpointing", Part A, sections 2,
-//    6.2 and 10, re-tiled for sm_103a (128-row tiles instead of 16).
+//    6.2 and 10, re-tiled for sm_103a (256-row pair tiles instead of 16).
 //  * Down (W2): y[p] = h[p] W2[e], bf16 out.
 // The always-on shared expert is one more group whose A operand is x itself
 // (SwiGLU) or the shared rows of h (down), and whose B operand is its own
 // weights; its outputs go to rows S .. S + T of h / y.
 //
 // Ragged groups: group g owns rows [row0_g, row0_g + n_g).  Its m-tiles load
-// 128 rows with TMA starting at row0_g + 128 m; rows past the group belong to
+// 256 rows with TMA starting at row0_g + 256 m; rows past the group belong to
 // the next group (or are zero-filled past the tensor) and are simply not
-// stored: the epilogue predicates each row.  The tile schedule is derived on
-// the device from the offsets (no host synchronisation): tiles are numbered
-// group by group, n fastest, and CTA b takes tiles b, b + grid, ...
+// stored: the epilogue predicates each row (and each 32-column chunk past N).
+// The tile schedule is derived on the device from the offsets (no host
+// synchronisation): tiles are numbered group by group, n fastest, and pair c
+// takes tiles c, c + pairs, ...
 //
-// Warp roles (320 threads, one CTA per SM):
-//   warp 0     TMA producer (one lane)
-//   warp 1     TMEM allocator + MMA issuer (one lane)
+// CTA pair: CTA r holds rows [128 r, 128 r + 128) of the A tile and columns
+// [r N/2, (r+1) N/2) of the B tile; the leader (r = 0) issues one
+// tcgen05.mma.cta_group::2 per 16-deep k-slice, which writes each CTA's 128
+// rows of D into that CTA's own TMEM.  Per SM, a 128x256 output tile then
+// stages 16 KB of A and 16 KB of B per 64-deep k-block instead of 16 + 32 KB.
+//
+// Warp roles (320 threads per CTA, one CTA per SM):
+//   warp 0     TMA producer (one lane) -- both CTAs load their own halves
+//   warp 1     TMEM allocator; MMA issuer (one lane, leader only)
 //   warps 2-9  epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 and the
 //              columns of half (w - 2) / 4 of the tile
-// Pipelines: kStages shared-memory stages (full / empty mbarriers) and two
-// TMEM accumulators of 256 columns (tmem_full / tmem_empty), so the epilogue
-// of one tile overlaps the MMAs of the next.
+// Pipelines: kPairStages shared-memory stages (full / empty mbarriers) and
+// two TMEM accumulators of 256 columns (tmem_full / tmem_empty), so the
+// epilogue of one tile overlaps the MMAs of the next.
 //
 // Shared-memory operand layouts (TMA, 128-byte swizzle):
 //   A tile 128 rows x 64 k (K-major): row r at byte 128 r, 8-row atoms of
 //     1024 bytes -> descriptor SBO = 1024; the k-th 16-wide slice starts
 //     32 k bytes into the tile.
-//   B tile 64 k x N (N-major, straight from the [K, N] row-major weights):
-//     N is split in 64-column boxes of 64 k-rows x 128 bytes (8 KB each);
+//   B tile 64 k x N/2 (N-major, straight from the [K, N] row-major weights):
+//     N/2 is split in 64-column boxes of 64 k-rows x 128 bytes (8 KB each);
 //     LBO = 8192 (next 64 columns), SBO = 1024 (next 8 k-rows); the k-th
 //     16-deep slice starts 2048 k bytes into the tile.
 #include <cudaTypedefs.h>
@@ -48,17 +56,11 @@ namespace moe {
 
 namespace {
 
-constexpr int kBM = 128;                      // rows per tile (TMEM lanes)
 constexpr int kBK = 64;                       // k per stage (128 bytes of bf16)
-constexpr int kStages = 4;
-constexpr int kABytes = kBM * kBK * 2;        // 16 KB
-constexpr int kBBytesMax = 256 * kBK * 2;     // 32 KB
-constexpr int kStageBytes = kABytes + kBBytesMax;
 constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kMaxGroups = MOE_MAX_EXPERTS + 1;
 constexpr uint32_t kTmemCols = 512;           // two 256-column accumulators
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;
 
 __device__ unsigned int g_device_error = 0;
 
@@ -74,9 +76,23 @@ struct GemmArgs {
   uint16_t* C;             // output [S + T_shared, N]
 };
 
-struct Ctl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+
+// ---------------------------------------------------------------------------
+// Barriers: full[s] lives in the leader and counts both CTAs' TMA bytes;
+// empty[s] and tfull[b] live in both CTAs and are signalled by the leader's
+// multicast commit; tempty[b] lives in the leader and counts the epilogue
+// warps of both CTAs.
+// ---------------------------------------------------------------------------
+constexpr int kPairBM = 256;                  // rows per pair tile
+constexpr int kPairStages = 6;
+constexpr int kPairABytes = 128 * kBK * 2;    // 16 KB: this CTA's 128 rows
+constexpr int kPairBBytesMax = 128 * kBK * 2; // 16 KB: this CTA's half of N <= 256
+constexpr int kPairStageBytes = kPairABytes + kPairBBytesMax;
+constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + 1024;
+
+struct PairCtl {
+  uint64_t full[kPairStages];
+  uint64_t empty[kPairStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -90,25 +106,30 @@ struct Ctl {
 
 template <bool kSwiGLU>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
-                        const __grid_constant__ CUtensorMap mapA_sh,
-                        const __grid_constant__ CUtensorMap mapB0,
-                        const __grid_constant__ CUtensorMap mapB1,
-                        const __grid_constant__ CUtensorMap mapB0_sh,
-                        const __grid_constant__ CUtensorMap mapB1_sh, const GemmArgs p) {
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA,
+                             const __grid_constant__ CUtensorMap mapA_sh,
+                             const __grid_constant__ CUtensorMap mapB0,
+                             const __grid_constant__ CUtensorMap mapB1,
+                             const __grid_constant__ CUtensorMap mapB0_sh,
+                             const __grid_constant__ CUtensorMap mapB1_sh, const GemmArgs p) {
   extern __shared__ uint8_t gemm_smem_raw[];
-  __shared__ Ctl ctl;
+  __shared__ PairCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(gemm_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t smem_base = smem_u32(smem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0 = leader, 1 = peer
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(cluster_id_x());
+  const int npairs = static_cast<int>(num_clusters_x());
   const int G = p.E + (p.T_shared > 0 ? 1 : 0);
   const int hw = kSwiGLU ? p.tile_n / 2 : p.tile_n;  // output columns per tile
-  const int ntn = p.N / hw;
+  const int ntn = (p.N + hw - 1) / hw;
   const int nkb = p.K / kBK;
+  const int half_n = p.tile_n / 2;                    // B columns staged by this CTA
 
-  // ---- group table and tile prefix ----
+  // ---- group table and tile prefix (identical in both CTAs) ----
   for (int g = threadIdx.x; g < G; g += kThreads) {
     if (g < p.E) {
       const int a = p.offsets[g], b = p.offsets[g + 1];
@@ -121,11 +142,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (warp == 0) {
-    const int per = (G + 31) / 32;  // <= 5
+    const int per = (G + 31) / 32;
     int local = 0;
     for (int i = 0; i < per; ++i) {
       const int g = lane * per + i;
-      if (g < G) local += ((ctl.nrows[g] + kBM - 1) / kBM) * ntn;
+      if (g < G) local += ((ctl.nrows[g] + kPairBM - 1) / kPairBM) * ntn;
     }
     int incl = local;
 #pragma unroll
@@ -138,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g = lane * per + i;
       if (g < G) {
         ctl.tile_prefix[g] = run;
-        run += ((ctl.nrows[g] + kBM - 1) / kBM) * ntn;
+        run += ((ctl.nrows[g] + kPairBM - 1) / kPairBM) * ntn;
       }
     }
     if (lane == 31) {
@@ -146,13 +167,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ctl.total_tiles = incl;
     }
     if (lane == 0) {
-      for (int s = 0; s < kStages; ++s) {
-        mbar_init(smem_u32(&ctl.full[s]), 1);
-        mbar_init(smem_u32(&ctl.empty[s]), 1);
+      for (int st = 0; st < kPairStages; ++st) {
+        mbar_init(smem_u32(&ctl.full[st]), 1);
+        mbar_init(smem_u32(&ctl.empty[st]), 1);
       }
       for (int b = 0; b < 2; ++b) {
         mbar_init(smem_u32(&ctl.tfull[b]), 1);
-        mbar_init(smem_u32(&ctl.tempty[b]), kEpiWarps);
+        mbar_init(smem_u32(&ctl.tempty[b]), 2 * kEpiWarps);
       }
       mbar_init(smem_u32(&ctl.drain), 1);
       ctl.abort = 0;
@@ -160,11 +181,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl.tmem_base), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&ctl.tmem_base), kTmemCols);
+    tmem_relinquish_pair();
     tc_fence_before_sync();
   }
-  __syncthreads();
+  // barrier inits and TMEM allocation visible to both CTAs before any use
+  cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl.tmem_base;
   const int total = ctl.total_tiles;
@@ -172,144 +194,146 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned int* dev_err = &g_device_error;
 
   if (warp == 0) {
-    // ===================== TMA producer =====================
+    // ===================== TMA producer (both CTAs) =====================
     if (lane == 0) {
       tma_prefetch_desc(&mapA);
       tma_prefetch_desc(&mapB0);
       if (kSwiGLU) tma_prefetch_desc(&mapB1);
       const uint64_t pol_a = l2_policy_evict_normal();
       const uint64_t pol_b = l2_policy_evict_last();
-      const uint32_t stage_tx = static_cast<uint32_t>(kABytes + p.tile_n * kBK * 2);
+      const uint32_t pair_tx = 2u * static_cast<uint32_t>(kPairABytes + half_n * kBK * 2);
       int stage = 0;
       uint32_t phase = 0;
       int g = 0;
       int issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = pair; tile < total && ok; tile += npairs) {
         while (tile >= ctl.tile_prefix[g + 1]) ++g;
         const int local = tile - ctl.tile_prefix[g];
         const int m = local / ntn, n = local - m * ntn;
         const bool routed = g < p.E;
         const CUtensorMap* mA = routed ? &mapA : &mapA_sh;
-        const CUtensorMap* mB0 = routed ? &mapB0 : &mapB0_sh;
-        const CUtensorMap* mB1 = routed ? &mapB1 : &mapB1_sh;
-        const int a_row = (routed ? ctl.row0[g] : p.shared_a_row0) + m * kBM;
+        const int a_row = (routed ? ctl.row0[g] : p.shared_a_row0) + m * kPairBM + 128 * rank;
         const int b_row0 = routed ? g * p.K : 0;
+        // this CTA's B columns
+        const CUtensorMap* mB;
+        int bcol;
+        if (kSwiGLU) {
+          mB = leader ? (routed ? &mapB0 : &mapB0_sh) : (routed ? &mapB1 : &mapB1_sh);
+          bcol = n * hw;
+        } else {
+          mB = routed ? &mapB0 : &mapB0_sh;
+          bcol = n * hw + half_n * rank;
+        }
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(smem_u32(&ctl.empty[stage]), phase ^ 1u, abort_flag, dev_err)) {
+          if (!mbar_wait_cluster(smem_u32(&ctl.empty[stage]), phase ^ 1u, abort_flag, dev_err)) {
             ok = false;
             break;
           }
-          const uint32_t full = smem_u32(&ctl.full[stage]);
-          const uint32_t sa = smem_base + stage * kStageBytes;
-          const uint32_t sb = sa + kABytes;
-          mbar_arrive_expect_tx(full, stage_tx);
-          tma_load_2d(sa, mA, full, kb * kBK, a_row, pol_a);
+          const uint32_t full_leader = map_to_cta(smem_u32(&ctl.full[stage]), 0);
+          const uint32_t sa = smem_base + stage * kPairStageBytes;
+          const uint32_t sb = sa + kPairABytes;
+          if (leader) mbar_arrive_expect_tx(smem_u32(&ctl.full[stage]), pair_tx);
+          tma_load_2d_pair(sa, mA, full_leader, kb * kBK, a_row, pol_a);
           const int brow = b_row0 + kb * kBK;
-          if (kSwiGLU) {
-            const int nch = hw / 64;
-            for (int cch = 0; cch < nch; ++cch) {
-              tma_load_2d(sb + cch * 8192, mB0, full, n * hw + cch * 64, brow, pol_b);
-              tma_load_2d(sb + (nch + cch) * 8192, mB1, full, n * hw + cch * 64, brow, pol_b);
-            }
-          } else {
-            const int nch = p.tile_n / 64;
-            for (int cch = 0; cch < nch; ++cch)
-              tma_load_2d(sb + cch * 8192, mB0, full, n * hw + cch * 64, brow, pol_b);
-          }
+          for (int cch = 0; cch < half_n / 64; ++cch)
+            tma_load_2d_pair(sb + cch * 8192, mB, full_leader, bcol + cch * 64, brow, pol_b);
           ++issued;
-          if (++stage == kStages) {
+          if (++stage == kPairStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok) {
+      if (!ok && leader) {
         // Let the copies already in flight land before the CTA exits.
         int st = stage;
         uint32_t ph = phase;
-        for (int i = 0; i < kStages && i < issued; ++i) {
+        for (int i = 0; i < kPairStages && i < issued; ++i) {
           if (--st < 0) {
-            st = kStages - 1;
+            st = kPairStages - 1;
             ph ^= 1u;
           }
           volatile int local_abort = 0;
-          mbar_wait(smem_u32(&ctl.full[st]), ph, &local_abort, dev_err);
+          mbar_wait_cluster(smem_u32(&ctl.full[st]), ph, &local_abort, dev_err);
         }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ===================== MMA issuer =====================
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(p.tile_n), 1u);
+    // ===================== MMA issuer (leader only) =====================
+    if (lane == 0 && leader) {
+      const uint32_t idesc = idesc_bf16_f32(kPairBM, static_cast<uint32_t>(p.tile_n), 1u);
       int stage = 0;
       uint32_t phase = 0;
       int i = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++i) {
+      for (int tile = pair; tile < total && ok; tile += npairs, ++i) {
         const int buf = i & 1;
         const uint32_t tph = (i >> 1) & 1;
-        if (!mbar_wait(smem_u32(&ctl.tempty[buf]), tph ^ 1u, abort_flag, dev_err)) break;
+        if (!mbar_wait_cluster(smem_u32(&ctl.tempty[buf]), tph ^ 1u, abort_flag, dev_err)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + buf * 256;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag, dev_err)) {
+          if (!mbar_wait_cluster(smem_u32(&ctl.full[stage]), phase, abort_flag, dev_err)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t sa = smem_base + stage * kStageBytes;
-          const uint32_t sb = sa + kABytes;
+          const uint32_t sa = smem_base + stage * kPairStageBytes;
+          const uint32_t sb = sa + kPairABytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bdesc = smem_desc_sw128(sb + kk * 2048, 8192, 1024);
-            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(smem_u32(&ctl.empty[stage]));
-          if (++stage == kStages) {
+          umma_commit_pair(smem_u32(&ctl.empty[stage]), 0x3);
+          if (++stage == kPairStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(smem_u32(&ctl.tfull[buf]));
+        umma_commit_pair(smem_u32(&ctl.tfull[buf]), 0x3);
       }
       // All MMAs issued by this thread are complete once `drain` flips.
-      umma_commit(smem_u32(&ctl.drain));
+      umma_commit_pair(smem_u32(&ctl.drain), 0x1);
       volatile int local_abort = 0;
-      mbar_wait(smem_u32(&ctl.drain), 0, &local_abort, dev_err);
+      mbar_wait_cluster(smem_u32(&ctl.drain), 0, &local_abort, dev_err);
     }
     __syncwarp();
   } else {
-    // ===================== epilogue =====================
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;  // which half of the tile's columns
-    const int r_in_tile = q * 32 + lane;
+    // ===================== epilogue (both CTAs) =====================
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int r_in_tile = 128 * static_cast<int>(rank) + q * 32 + lane;
+    const uint32_t tempty_leader0 = map_to_cta(smem_u32(&ctl.tempty[0]), 0);
+    const uint32_t tempty_leader1 = map_to_cta(smem_u32(&ctl.tempty[1]), 0);
     int g = 0;
     int i = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++i) {
+    for (int tile = pair; tile < total; tile += npairs, ++i) {
       while (tile >= ctl.tile_prefix[g + 1]) ++g;
       const int local = tile - ctl.tile_prefix[g];
       const int m = local / ntn, n = local - m * ntn;
       const int buf = i & 1;
       const uint32_t tph = (i >> 1) & 1;
-      const bool got = mbar_wait(smem_u32(&ctl.tfull[buf]), tph, abort_flag, dev_err);
+      const bool got = mbar_wait_cluster(smem_u32(&ctl.tfull[buf]), tph, abort_flag, dev_err);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
-      const int row = m * kBM + r_in_tile;
+      const int row = m * kPairBM + r_in_tile;
       const bool valid = row < ctl.nrows[g];
-      uint16_t* crow = p.C + static_cast<size_t>(ctl.row0[g] + (valid ? row : 0)) * p.N + n * hw;
+      const int col0 = n * hw;
+      uint16_t* crow = p.C + static_cast<size_t>(ctl.row0[g] + (valid ? row : 0)) * p.N + col0;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * 256;
       const int c_lo = half * (hw / 2), c_hi = c_lo + hw / 2;
-      if (kSwiGLU) {
-        for (int cc = c_lo; cc < c_hi; cc += 32) {
+      for (int cc = c_lo; cc < c_hi; cc += 32) {
+        uint32_t packed[16];
+        if (kSwiGLU) {
           uint32_t rg[32], ru[32];
           tmem_ld_32cols(taddr + cc, rg);
           tmem_ld_32cols(taddr + hw + cc, ru);
           tmem_ld_wait();
-          uint32_t packed[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float g0 = __uint_as_float(rg[2 * j]), g1 = __uint_as_float(rg[2 * j + 1]);
@@ -320,40 +344,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
             packed[j] = pack_bf16x2(h0, h1);
           }
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(crow + cc);
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-          }
-        }
-      } else {
-        for (int cc = c_lo; cc < c_hi; cc += 32) {
+        } else {
           uint32_t ra[32];
           tmem_ld_32cols(taddr + cc, ra);
           tmem_ld_wait();
-          uint32_t packed[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             packed[j] = pack_bf16x2(__uint_as_float(ra[2 * j]), __uint_as_float(ra[2 * j + 1]));
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(crow + cc);
+        }
+        if (valid && col0 + cc < p.N) {
+          uint4* dst = reinterpret_cast<uint4*>(crow + cc);
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-          }
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
         }
       }
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl.tempty[buf]));
+      if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
     }
   }
 
-  __syncthreads();
+  // Both CTAs done with TMEM and with each other's barriers before freeing.
+  tc_fence_before_sync();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -391,9 +408,29 @@ cudaError_t make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t co
 struct DeviceInfo {
   int device = -1;
   int sms = 0;
+  int pair_clusters[2] = {0, 0};  // co-resident CTA pairs: [down, swiglu]
   bool attrs_set = false;
 };
 DeviceInfo g_dev[64];
+
+template <bool kSwiGLU>
+cudaError_t launch_pair(int nclusters, const CUtensorMap& a, const CUtensorMap& as,
+                        const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b0s,
+                        const CUtensorMap& b1s, const GemmArgs& args, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * nclusters, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPairSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kSwiGLU>, a, as, b0, b1, b0s, b1s, args);
+}
 
 cudaError_t device_setup(int* sms) {
   int dev = 0;
@@ -404,16 +441,38 @@ cudaError_t device_setup(int* sms) {
   if (!di.attrs_set) {
     e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(grouped_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(grouped_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
-    if (e != cudaSuccess) return e;
+    for (int sw = 0; sw < 2; ++sw) {
+      const void* fn = sw ? reinterpret_cast<const void*>(grouped_gemm_pair_kernel<true>)
+                          : reinterpret_cast<const void*>(grouped_gemm_pair_kernel<false>);
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
+      if (e != cudaSuccess) return e;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (di.sms / 2), 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = kPairSmemBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int nclusters = 0;
+      e = cudaOccupancyMaxActiveClusters(&nclusters, fn, &cfg);
+      if (e != cudaSuccess) return e;
+      if (nclusters < 1) return cudaErrorInvalidConfiguration;
+      di.pair_clusters[sw] = nclusters;
+    }
     di.attrs_set = true;
   }
   *sms = di.sms;
   return cudaSuccess;
+}
+
+int pair_clusters(bool swiglu) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return g_dev[dev].pair_clusters[swiglu ? 1 : 0];
 }
 
 }  // namespace
@@ -428,13 +487,13 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
   if ((e = device_setup(&sms)) != cudaSuccess) return e;
   const int S = d.T * d.k;
   const bool shared = Ws1 != nullptr;
-  const int hw = (d.F % 128 == 0) ? 128 : 64;
+  const int hw = 128;  // the last tile is half empty when F % 128 == 64
   CUtensorMap mA, mAs, mB0, mB1, mB0s, mB1s;
-  if ((e = make_map(&mA, x_sorted, S, d.D, kBM, kBK)) != cudaSuccess) return e;
+  if ((e = make_map(&mA, x_sorted, S, d.D, 128, kBK)) != cudaSuccess) return e;
   if ((e = make_map(&mB0, W1, static_cast<uint64_t>(d.E) * d.D, d.F, kBK, 64)) != cudaSuccess) return e;
   if ((e = make_map(&mB1, W3, static_cast<uint64_t>(d.E) * d.D, d.F, kBK, 64)) != cudaSuccess) return e;
   if (shared) {
-    if ((e = make_map(&mAs, x, d.T, d.D, kBM, kBK)) != cudaSuccess) return e;
+    if ((e = make_map(&mAs, x, d.T, d.D, 128, kBK)) != cudaSuccess) return e;
     if ((e = make_map(&mB0s, Ws1, d.D, d.F, kBK, 64)) != cudaSuccess) return e;
     if ((e = make_map(&mB1s, Ws3, d.D, d.F, kBK, 64)) != cudaSuccess) return e;
   } else {
@@ -452,9 +511,9 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
   a.tile_n = 2 * hw;
   a.shared_a_row0 = 0;
   a.C = h;
-  grouped_gemm_kernel<true><<<sms, kThreads, kSmemBytes, s>>>(mA, mAs, mB0, mB1, mB0s, mB1s, a);
+  e = launch_pair<true>(pair_clusters(true), mA, mAs, mB0, mB1, mB0s, mB1s, a, s);
   note_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uint16_t* Ws2,
@@ -466,10 +525,11 @@ cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uin
   if ((e = device_setup(&sms)) != cudaSuccess) return e;
   const int S = d.T * d.k;
   const bool shared = Ws2 != nullptr;
-  const int tn = (d.D % 256 == 0) ? 256 : (d.D % 128 == 0) ? 128 : 64;
+  // D % 128 == 64: 128-wide tiles, the last one half empty
+  const int tn = (d.D % 256 == 0) ? 256 : 128;
   const uint64_t hrows = static_cast<uint64_t>(S) + (shared ? d.T : 0);
   CUtensorMap mA, mB0, mB0s;
-  if ((e = make_map(&mA, h, hrows, d.F, kBM, kBK)) != cudaSuccess) return e;
+  if ((e = make_map(&mA, h, hrows, d.F, 128, kBK)) != cudaSuccess) return e;
   if ((e = make_map(&mB0, W2, static_cast<uint64_t>(d.E) * d.F, d.D, kBK, 64)) != cudaSuccess) return e;
   if (shared) {
     if ((e = make_map(&mB0s, Ws2, d.F, d.D, kBK, 64)) != cudaSuccess) return e;
@@ -486,9 +546,9 @@ cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uin
   a.tile_n = tn;
   a.shared_a_row0 = S;
   a.C = y;
-  grouped_gemm_kernel<false><<<sms, kThreads, kSmemBytes, s>>>(mA, mA, mB0, mB0, mB0s, mB0s, a);
+  e = launch_pair<false>(pair_clusters(false), mA, mA, mB0, mB0, mB0s, mB0s, a, s);
   note_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t read_clear_device_error(unsigned int* value) {

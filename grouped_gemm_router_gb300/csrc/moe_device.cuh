@@ -10,9 +10,8 @@
 
 #define MOE_DEV __device__ __forceinline__
 
-// Device error word (one per device), set by kernels whose on-chip waits time
-// out.  Defined in moe_api.cu (relocatable device code is not used, so each
-// translation unit that needs it gets a pointer to it as a kernel argument).
+// Bit set in the device error word (defined in grouped_gemm.cu, read and
+// cleared by moe_device_error) when an on-chip wait times out.
 #define MOE_DEVERR_TIMEOUT 1u
 
 // A wait on an on-chip barrier is abandoned after this long.
@@ -81,6 +80,81 @@ MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
   }
 }
 
+// Same as mbar_try_wait with acquire semantics at cluster scope (for barriers
+// that receive arrivals from the peer CTA of a cluster).
+MOE_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait as mbar_wait, at cluster scope.
+MOE_DEV bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort,
+                               unsigned int* dev_err) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > MOE_WAIT_TIMEOUT_NS) {
+        *abort = 1;
+        atomicOr(dev_err, MOE_DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Arrive on a barrier given by its shared::cluster address (possibly in the
+// peer CTA), release at cluster scope.
+MOE_DEV void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Clusters
+// ---------------------------------------------------------------------------
+MOE_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+MOE_DEV uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+
+MOE_DEV uint32_t num_clusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+
+// shared::cluster address of the variable at shared::cta address `addr` in
+// the CTA of rank `rank` of this cluster.
+MOE_DEV uint32_t map_to_cta(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// All threads of all CTAs of the cluster.
+MOE_DEV void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), 2-D tiles into shared memory
 // ---------------------------------------------------------------------------
@@ -96,6 +170,17 @@ MOE_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(cache_policy)
+      : "memory");
+}
+
+// As tma_load_2d for a CTA pair: `bar` is a shared::cluster address, which may
+// be the barrier of the peer CTA.
+MOE_DEV void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                              int32_t c1, uint64_t cache_policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(cache_policy)
       : "memory");
 }
@@ -129,6 +214,44 @@ MOE_DEV void tmem_relinquish() {
 MOE_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
+}
+
+// CTA-pair forms (cta_group::2): both CTAs of the pair allocate / free the
+// same columns of their own TMEM together.
+MOE_DEV void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+
+MOE_DEV void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+MOE_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// One MMA over the CTA pair: A rows split between the two CTAs (M / 2 each),
+// B columns split (N / 2 each), D rows in each CTA's own TMEM.
+MOE_DEV void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the barrier at shared::cta offset `bar` in every CTA of
+// `cta_mask` when the pair MMAs issued so far by this thread complete.
+MOE_DEV void umma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar), "h"(cta_mask)
+      : "memory");
 }
 
 MOE_DEV void tc_fence_before_sync() {
