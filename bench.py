@@ -9,10 +9,12 @@ all inputs resident in HBM.  One JSON line is printed by rank 0.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 
 Timing: W untimed warm-up steps; then K steps, each bracketed by CUDA events
-on the launching stream, with a 512 MB buffer written between steps to flush
-the 129 MB L2 (outside the events).  Multi-GPU (torchrun): every rank runs its
-own replica of the layer on its own batch (weak scaling, no collective on the
-data path); the step time is the max over ranks.
+on the launching stream.  Between steps (outside the events) a 512 MB buffer
+is written and then read back, so each step starts with a cold L2 that holds
+no dirty lines of the flush (their write-back is not charged to the step).
+Multi-GPU (torchrun): every rank runs its own replica of the layer on its own
+batch (weak scaling, no collective on the data path); the step time is the max
+over ranks.
 
 --impl reference times the fp64 CPU oracle as it stands on the host cores,
 on a bounded sample of the same workload, and prints the same line with
@@ -269,7 +271,12 @@ def main():
     T, D, F, E, k = w.T, w.D, w.F, w.E, w.k
     ws = moe.Workspace(T, D, F, E, k, w.shared, device=dev)
     out = torch.empty(T, D, dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        flush.fill_(1)
+        flush_sink.copy_(flush.sum(dtype=torch.int64))
 
     def step(events=None):
         moe.moe_ffn_forward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], k, bias=G["bias"],
@@ -277,7 +284,7 @@ def main():
                             stage_events=events)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
     torch.cuda.synchronize()
     if moe.device_error() != 0:
@@ -285,6 +292,9 @@ def main():
 
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for row in evs:  # create the CUDA events now, outside the timed loop
+        for ev in row:
+            ev.record()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -292,7 +302,7 @@ def main():
     n_launch0 = moe.launch_count()
     wall0 = time.perf_counter()
     for i in range(K):
-        flush.zero_()
+        flush_l2()
         step(evs[i])
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -316,7 +326,9 @@ def main():
     for i in range(args.warmup + K2):
         ev = [None] * 8
         ev[6], ev[7] = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        flush.zero_()
+        ev[6].record()
+        ev[7].record()
+        flush_l2()
         moe.moe_ffn_forward_host(x_host, G["Wg"], G["W1"], G["W3"], G["W2"], k, out_host, ws_h,
                                  bias=G["bias"], Ws1=G["Ws1"], Ws3=G["Ws3"], Ws2=G["Ws2"],
                                  stage_events=ev)
@@ -352,7 +364,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "D": w.D, "F": w.F, "E": w.E, "k": w.k,
-                   "shared_expert": w.shared, "l2": "flushed between steps (512 MB write)",
+                   "shared_expert": w.shared, "l2": "flushed between steps (512 MB write + read back)",
                    "parallelism": f"replicas x{world}"},
         "active_tflops": fl * world / (ms / 1e3) / 1e12,
         "frac_of_bf16_peak": fl / (ms / 1e3) / 1e12 / pk["bf16_tflops"],

@@ -23,7 +23,6 @@ MOE_ERR_DEVICE_TIMEOUT = -5
 MAX_EXPERTS = 128
 MAX_TOPK = 16
 MAX_DIM = 8192
-ROUTE_BLOCK_TOKENS = 64
 
 
 class MoeDims(ctypes.Structure):
@@ -52,6 +51,7 @@ _SIGNATURES = {
     "moe_ffn_forward_host": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, MoeDims, _vp, _vp,
                                     _sz, ctypes.POINTER(MoeOptions), _vp]),
     "moe_route": (_i32, [_vp, _vp, _vp, MoeDims, _vp, _vp, _vp, _vp]),
+    "moe_route_block_tokens": (_i32, [_i32]),
     "moe_permute_scratch_size": (_sz, [MoeDims]),
     "moe_permute": (_i32, [_vp, MoeDims, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_grouped_swiglu": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, MoeDims, _vp, _vp]),
@@ -91,3 +91,9 @@ def check(status: int, where: str) -> None:
 
 def dims(T: int, D: int, F: int, E: int, k: int) -> MoeDims:
     return MoeDims(T, D, F, E, k)
+
+
+def route_blocks(T: int) -> int:
+    """Blocks of the router / permutation kernels (rows of the block histogram)."""
+    tb = int(lib.moe_route_block_tokens(T))
+    return (T + tb - 1) // tb

@@ -88,7 +88,9 @@ constexpr int kPairStages = 6;
 constexpr int kPairABytes = 128 * kBK * 2;    // 16 KB: this CTA's 128 rows
 constexpr int kPairBBytesMax = 128 * kBK * 2; // 16 KB: this CTA's half of N <= 256
 constexpr int kPairStageBytes = kPairABytes + kPairBBytesMax;
-constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + 1024;
+constexpr int kOutBoxRows = 32;                 // one epilogue warp's rows
+constexpr int kOutBoxBytes = kOutBoxRows * 128;  // 32 rows x 64 bf16 columns
+constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + kEpiWarps * kOutBoxBytes + 1024;
 
 struct PairCtl {
   uint64_t full[kPairStages];
@@ -111,7 +113,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                              const __grid_constant__ CUtensorMap mapB0,
                              const __grid_constant__ CUtensorMap mapB1,
                              const __grid_constant__ CUtensorMap mapB0_sh,
-                             const __grid_constant__ CUtensorMap mapB1_sh, const GemmArgs p) {
+                             const __grid_constant__ CUtensorMap mapB1_sh,
+                             const __grid_constant__ CUtensorMap mapC, const GemmArgs p) {
   extern __shared__ uint8_t gemm_smem_raw[];
   __shared__ PairCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -305,11 +308,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ===================== epilogue (both CTAs) =====================
+    // Warp w owns TMEM lanes 32 (w % 4) .. + 31 (32 output rows) and half
+    // (w - 2) / 4 of the tile's columns, in boxes of 64 columns.  A box whose
+    // 32 rows all belong to the group is written through a 128B-swizzled
+    // staging buffer with one TMA store (full 128-byte lines); a box that
+    // crosses the group's end is stored row by row for its valid rows only.
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r_in_tile = 128 * static_cast<int>(rank) + q * 32 + lane;
     const uint32_t tempty_leader0 = map_to_cta(smem_u32(&ctl.tempty[0]), 0);
     const uint32_t tempty_leader1 = map_to_cta(smem_u32(&ctl.tempty[1]), 0);
+    uint8_t* stage_out = smem + kPairStages * kPairStageBytes + (warp - 2) * kOutBoxBytes;
+    const uint32_t stage_out_u32 = smem_u32(stage_out);
     int g = 0;
     int i = 0;
     for (int tile = pair; tile < total; tile += npairs, ++i) {
@@ -322,47 +332,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
       const int row = m * kPairBM + r_in_tile;
-      const bool valid = row < ctl.nrows[g];
+      const int nrows_g = ctl.nrows[g];
+      const bool valid = row < nrows_g;
+      const int warp_row0 = m * kPairBM + 128 * static_cast<int>(rank) + q * 32;
+      const bool full_box = warp_row0 + kOutBoxRows <= nrows_g;
       const int col0 = n * hw;
       uint16_t* crow = p.C + static_cast<size_t>(ctl.row0[g] + (valid ? row : 0)) * p.N + col0;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * 256;
-      const int c_lo = half * (hw / 2), c_hi = c_lo + hw / 2;
-      for (int cc = c_lo; cc < c_hi; cc += 32) {
-        uint32_t packed[16];
-        if (kSwiGLU) {
-          uint32_t rg[32], ru[32];
-          tmem_ld_32cols(taddr + cc, rg);
-          tmem_ld_32cols(taddr + hw + cc, ru);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float g0 = __uint_as_float(rg[2 * j]), g1 = __uint_as_float(rg[2 * j + 1]);
-            const float u0 = __uint_as_float(ru[2 * j]), u1 = __uint_as_float(ru[2 * j + 1]);
-            // silu(g) = g / (1 + exp(-g)); the fast division returns 0 when
-            // exp(-g) overflows, which is the limit of silu for g -> -inf.
-            const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
-            const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
-            packed[j] = pack_bf16x2(h0, h1);
-          }
-        } else {
-          uint32_t ra[32];
-          tmem_ld_32cols(taddr + cc, ra);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            packed[j] = pack_bf16x2(__uint_as_float(ra[2 * j]), __uint_as_float(ra[2 * j + 1]));
+      for (int bc = half * (hw / 2); bc < (half + 1) * (hw / 2); bc += 64) {
+        if (col0 + bc >= p.N) break;  // box past the last column (half-empty last tile)
+        if (full_box) {
+          bulk_wait_group_read0();  // the previous box's store has read the staging buffer
+          __syncwarp();
         }
-        if (valid && col0 + cc < p.N) {
-          uint4* dst = reinterpret_cast<uint4*>(crow + cc);
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+        for (int cc2 = 0; cc2 < 64; cc2 += 32) {
+          const int cc = bc + cc2;
+          uint32_t packed[16];
+          if (kSwiGLU) {
+            uint32_t rg[32], ru[32];
+            tmem_ld_32cols(taddr + cc, rg);
+            tmem_ld_32cols(taddr + hw + cc, ru);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float g0 = __uint_as_float(rg[2 * j]), g1 = __uint_as_float(rg[2 * j + 1]);
+              const float u0 = __uint_as_float(ru[2 * j]), u1 = __uint_as_float(ru[2 * j + 1]);
+              // silu(g) = g / (1 + exp(-g)); the fast division returns 0 when
+              // exp(-g) overflows, which is the limit of silu for g -> -inf.
+              const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+              const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
+              packed[j] = pack_bf16x2(h0, h1);
+            }
+          } else {
+            uint32_t ra[32];
+            tmem_ld_32cols(taddr + cc, ra);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              packed[j] = pack_bf16x2(__uint_as_float(ra[2 * j]), __uint_as_float(ra[2 * j + 1]));
+          }
+          if (full_box) {
+            // 16-byte chunk c of this lane's 128-byte row goes to chunk c ^ (row % 8)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int chunk = (cc2 >> 3) + v;
+              uint4* dst = reinterpret_cast<uint4*>(stage_out + lane * 128 + ((chunk ^ (lane & 7)) << 4));
+              *dst = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+            }
+          } else if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(crow + cc);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+          }
+        }
+        if (full_box) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&mapC, stage_out_u32, col0 + bc, ctl.row0[g] + warp_row0);
+            bulk_commit_group();
+          }
         }
       }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
     }
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
   }
 
   // Both CTAs done with TMEM and with each other's barriers before freeing.
@@ -416,7 +455,8 @@ DeviceInfo g_dev[64];
 template <bool kSwiGLU>
 cudaError_t launch_pair(int nclusters, const CUtensorMap& a, const CUtensorMap& as,
                         const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b0s,
-                        const CUtensorMap& b1s, const GemmArgs& args, cudaStream_t s) {
+                        const CUtensorMap& b1s, const CUtensorMap& c, const GemmArgs& args,
+                        cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * nclusters, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -429,7 +469,7 @@ cudaError_t launch_pair(int nclusters, const CUtensorMap& a, const CUtensorMap& 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kSwiGLU>, a, as, b0, b1, b0s, b1s, args);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kSwiGLU>, a, as, b0, b1, b0s, b1s, c, args);
 }
 
 cudaError_t device_setup(int* sms) {
@@ -511,7 +551,11 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
   a.tile_n = 2 * hw;
   a.shared_a_row0 = 0;
   a.C = h;
-  e = launch_pair<true>(pair_clusters(true), mA, mAs, mB0, mB1, mB0s, mB1s, a, s);
+  CUtensorMap mC;
+  if ((e = make_map(&mC, h, static_cast<uint64_t>(S) + (shared ? d.T : 0), d.F, kOutBoxRows, 64)) !=
+      cudaSuccess)
+    return e;
+  e = launch_pair<true>(pair_clusters(true), mA, mAs, mB0, mB1, mB0s, mB1s, mC, a, s);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -546,7 +590,9 @@ cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uin
   a.tile_n = tn;
   a.shared_a_row0 = S;
   a.C = y;
-  e = launch_pair<false>(pair_clusters(false), mA, mA, mB0, mB0, mB0s, mB0s, a, s);
+  CUtensorMap mC;
+  if ((e = make_map(&mC, y, hrows, d.D, kOutBoxRows, 64)) != cudaSuccess) return e;
+  e = launch_pair<false>(pair_clusters(false), mA, mA, mB0, mB0, mB0s, mB0s, mC, a, s);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }

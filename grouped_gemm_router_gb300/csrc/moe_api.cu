@@ -207,6 +207,8 @@ moe_status moe_route(const void* x, const void* Wg, const float* router_bias, mo
                                   static_cast<cudaStream_t>(stream)));
 }
 
+int moe_route_block_tokens(int T) { return route_block_tokens(T); }
+
 size_t moe_permute_scratch_size(moe_dims d) {
   if (check_dims(d) != MOE_OK) return 0;
   return static_cast<size_t>(route_blocks(d.T)) * d.E * 4;

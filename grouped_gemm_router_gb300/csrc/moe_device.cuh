@@ -185,6 +185,31 @@ MOE_DEV void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar
       : "memory");
 }
 
+// Stores the 2-D box at coordinates (c0, c1) from shared memory at `src`
+// (bulk async group of the executing thread).  c0 * element size must be a
+// multiple of 16 bytes and neither coordinate may be negative.
+MOE_DEV void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(src)
+               : "memory");
+}
+
+MOE_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until no bulk group of this thread still reads shared memory.
+MOE_DEV void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Waits until all bulk groups of this thread have completed.
+MOE_DEV void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Makes generic-proxy shared-memory writes visible to the async proxy (TMA).
+MOE_DEV void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 MOE_DEV uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));

@@ -12,7 +12,8 @@ namespace moe {
 void note_launch();
 
 // ---- routing / permutation (route_permute.cu) ----
-int route_blocks(int T);  // ceil(T / MOE_ROUTE_BLOCK_TOKENS)
+int route_block_tokens(int T);  // tokens per router / permutation block (16, 32 or 64)
+int route_blocks(int T);        // ceil(T / route_block_tokens(T))
 cudaError_t launch_route(const uint16_t* x, const uint16_t* Wg, const float* bias, const moe_dims& d,
                          int32_t* ids, float* w, int32_t* hist, cudaStream_t s);
 cudaError_t launch_hist(const int32_t* ids, const moe_dims& d, int32_t* hist, cudaStream_t s);

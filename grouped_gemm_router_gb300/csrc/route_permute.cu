@@ -16,11 +16,21 @@
 
 namespace moe {
 
-constexpr int kRouteTokens = MOE_ROUTE_BLOCK_TOKENS;  // tokens per block
-constexpr int kRouteWarps = kRouteTokens / 16;        // one 16-token MMA tile per warp
+constexpr int kRouteThreads = 256;                    // 8 warps per router block
 constexpr int kRouteSmemBytes = 64 * 1024;            // staged router weights per D-chunk
 
-int route_blocks(int T) { return (T + kRouteTokens - 1) / kRouteTokens; }
+// Tokens per router / permutation block: 64 when that still gives every SM two
+// blocks, else 32 or 16, so that small batches spread over the whole GPU.
+int route_block_tokens(int T) {
+  if (T >= 64 * 2 * 152) return 64;
+  if (T >= 32 * 2 * 152) return 32;
+  return 16;
+}
+
+int route_blocks(int T) {
+  const int tb = route_block_tokens(T);
+  return (T + tb - 1) / tb;
+}
 
 MOE_DEV void mma_m16n8k16_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                uint32_t b0, uint32_t b1) {
@@ -31,9 +41,12 @@ MOE_DEV void mma_m16n8k16_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Block = 4 warps = 64 tokens.  Warp w owns tokens [t0, t0 + 16).  Lane
+// Block = 8 warps for TB = 16 MT tokens (MT = 1, 2 or 4 tiles of 16 tokens).
+// Warp w computes tile w % MT over the 32-wide D-chunks kc with
+// kc % DS == w / MT (DS = 8 / MT warps share a tile); their partial logits are
+// summed through shared memory before the selection.  Lane
 // (g = lane / 4, c = lane % 4) loads 16 bytes of rows g and g + 8 at columns
-// d + 8c .. d + 8c + 7 of every 32-wide chunk: a coalesced 64-byte segment per
+// d + 8c .. d + 8c + 7 of a 32-wide chunk: a coalesced 64-byte segment per
 // row.  The reduction order over d inside a chunk is irrelevant, so those 8
 // columns feed two m16n8k16 MMAs as their (2c, 2c+1, 2c+8, 2c+9) columns, and
 // the router weights are staged in shared memory in the matching order:
@@ -42,19 +55,26 @@ MOE_DEV void mma_m16n8k16_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t
 // Selection: thread (g, c) holds the logits of experts 8n + 2c + {0,1} for
 // rows g and g + 8.  Each of the k rounds takes the largest not-yet-chosen
 // logit (ties to the lower expert index) across the quad.
+// Resident blocks per SM the register budget is sized for: all blocks of a
+// 32K-token batch (512 blocks) fit in one wave for E <= 8.
+constexpr int route_min_blocks(int nt) { return nt <= 1 ? 4 : nt <= 2 ? 3 : nt <= 8 ? 2 : 1; }
+
 template <int NT>
-__global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(
+__global__ void __launch_bounds__(kRouteThreads, route_min_blocks(NT)) route_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ Wg, const float* __restrict__ bias,
-    int T, int D, int E, int k, int dchunk, int32_t* __restrict__ ids, float* __restrict__ wts,
-    int32_t* __restrict__ hist) {
+    int T, int D, int E, int k, int dchunk, int TB, int32_t* __restrict__ ids,
+    float* __restrict__ wts, int32_t* __restrict__ hist) {
   extern __shared__ __align__(16) uint8_t route_smem[];
   uint4* wpack = reinterpret_cast<uint4*>(route_smem);
   uint16_t* wpack16 = reinterpret_cast<uint16_t*>(route_smem);
+  float* red = reinterpret_cast<float*>(route_smem);  // reused after the D loop
   __shared__ int s_hist[MOE_MAX_EXPERTS];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int t0 = blockIdx.x * kRouteTokens + warp * 16;
+  const int MT = TB >> 4, DS = 8 / MT;
+  const int tile = warp % MT, split = warp / MT;
+  const int t0 = blockIdx.x * TB + tile * 16;
   const int row0 = t0 + g, row1 = t0 + g + 8;
   const bool ok0 = row0 < T, ok1 = row1 < T;
   const uint4* xr0 = reinterpret_cast<const uint4*>(x + static_cast<size_t>(ok0 ? row0 : 0) * D);
@@ -66,8 +86,8 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(
 #pragma unroll
   for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 
-  constexpr int EP = NT * 8;              // experts padded to whole MMA tiles
-  constexpr int KG = (NT >= 8) ? 4 : 8;   // 32-wide chunks loaded per batch
+  constexpr int EP = NT * 8;                            // experts padded to whole MMA tiles
+  constexpr int KG = (NT >= 8) ? 2 : 4;      // chunks per load batch
   for (int d0 = 0; d0 < D; d0 += dchunk) {
     const int dc = min(dchunk, D - d0);
     __syncthreads();
@@ -108,27 +128,47 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(
     }
     __syncthreads();
     const int nkc = dc >> 5;
-    for (int kc0 = 0; kc0 < nkc; kc0 += KG) {
+    for (int kc0 = split; kc0 < nkc; kc0 += KG * DS) {
       // all x loads of the batch first (2 rows x KG chunks of 16 bytes)
       uint4 a0[KG], a1[KG];
 #pragma unroll
       for (int j = 0; j < KG; ++j) {
-        const int q = ((d0 + (kc0 + j) * 32) >> 3) + c;  // 16-byte column index
-        const bool in = kc0 + j < nkc;
+        const int kc = kc0 + j * DS;
+        const int q = ((d0 + kc * 32) >> 3) + c;  // 16-byte column index
+        const bool in = kc < nkc;
         a0[j] = (ok0 && in) ? __ldg(xr0 + q) : make_uint4(0, 0, 0, 0);
         a1[j] = (ok1 && in) ? __ldg(xr1 + q) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int j = 0; j < KG; ++j) {
-        if (kc0 + j >= nkc) break;
+        const int kc = kc0 + j * DS;
+        if (kc >= nkc) break;
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          const uint4 b = wpack[(static_cast<size_t>(kc0 + j) * NT + n) * 32 + lane];
+          const uint4 b = wpack[(static_cast<size_t>(kc) * NT + n) * 32 + lane];
           mma_m16n8k16_bf16(acc[n], a0[j].x, a1[j].x, a0[j].y, a1[j].y, b.x, b.y);
           mma_m16n8k16_bf16(acc[n], a0[j].z, a1[j].z, a0[j].w, a1[j].w, b.z, b.w);
         }
       }
     }
+  }
+
+  // ---- sum the DS partial results of each tile (shared memory reused) ----
+  __syncthreads();
+  if (split > 0) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) red[((warp * NT + n) * 4 + i) * 32 + lane] = acc[n][i];
+  }
+  __syncthreads();
+  if (split > 0) return;
+  for (int sp = 1; sp < DS; ++sp) {
+    const int w2 = tile + sp * MT;
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[n][i] += red[((w2 * NT + n) * 4 + i) * 32 + lane];
   }
 
   // ---- top-k + softmax for rows g (r = 0) and g + 8 (r = 1) ----
@@ -204,20 +244,21 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(
       }
     }
   }
-  __syncthreads();
+  // only the MT selecting warps are left: sync them on a named barrier
+  asm volatile("bar.sync 1, %0;" ::"r"(MT * 32) : "memory");
   if (hist != nullptr)
-    for (int i = threadIdx.x; i < E; i += blockDim.x)
+    for (int i = threadIdx.x; i < E; i += MT * 32)
       hist[static_cast<size_t>(blockIdx.x) * E + i] = s_hist[i];
 }
 
-// Per-block expert histogram of given ids (same blocking as route_kernel).
+// Per-block expert histogram of given ids (blocks of TB tokens, as route_kernel).
 __global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ ids, int T, int k,
-                                                   int E, int32_t* __restrict__ hist) {
+                                                   int E, int TB, int32_t* __restrict__ hist) {
   __shared__ int s_hist[MOE_MAX_EXPERTS];
   for (int i = threadIdx.x; i < E; i += blockDim.x) s_hist[i] = 0;
   __syncthreads();
-  const int s0 = blockIdx.x * kRouteTokens * k;  // T * k <= 2^28 fits in int
-  const int ns = min(kRouteTokens * k, T * k - s0);
+  const int s0 = blockIdx.x * TB * k;  // T * k <= 2^28 fits in int
+  const int ns = min(TB * k, T * k - s0);
   for (int i = threadIdx.x; i < ns; i += blockDim.x) {
     const int e = ids[s0 + i];
     if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicAdd(&s_hist[e], 1);
@@ -227,7 +268,7 @@ __global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ i
     hist[static_cast<size_t>(blockIdx.x) * E + i] = s_hist[i];
 }
 
-// Scatter: block b owns the slots of tokens [64b, 64b + 64).
+// Scatter: block b owns the slots of tokens [TB b, TB b + TB).
 //  1. From the whole block histogram it forms counts, offsets (exclusive
 //     scan over experts) and this block's first position per expert
 //     (offsets[e] + the counts of expert e in blocks before b).
@@ -239,14 +280,15 @@ constexpr int kScatterThreads = 256;
 constexpr int kScatterWarps = kScatterThreads / 32;
 
 __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
-    const int32_t* __restrict__ ids, const int32_t* __restrict__ hist, int T, int k, int E, int nblk,
+    const int32_t* __restrict__ ids, const int32_t* __restrict__ hist, int T, int k, int E, int TB,
+    int nblk,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
     int32_t* __restrict__ inv, const uint4* __restrict__ x, uint4* __restrict__ xs, int D) {
   __shared__ int s_red_pre[kScatterThreads];
   __shared__ int s_red_tot[kScatterThreads];
   __shared__ int s_base[MOE_MAX_EXPERTS];
   __shared__ int s_wcnt[kScatterWarps][MOE_MAX_EXPERTS];
-  __shared__ int s_pos[kRouteTokens * MOE_MAX_TOPK];
+  __shared__ int s_pos[64 * MOE_MAX_TOPK];
 
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -308,8 +350,8 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
   }
 
   // ---- 2. stable ranks ----
-  const int s0 = b * kRouteTokens * k;
-  const int ns = min(kRouteTokens * k, S - s0);
+  const int s0 = b * TB * k;
+  const int ns = min(TB * k, S - s0);
   for (int base = 0; base < ns; base += kScatterThreads) {
     for (int i = tid; i < kScatterWarps * E; i += kScatterThreads) s_wcnt[i / E][i % E] = 0;
     __syncthreads();
@@ -383,12 +425,22 @@ static cudaError_t launch_route_nt(const uint16_t* x, const uint16_t* Wg, const 
   int dchunk = kRouteSmemBytes / (NT * 8 * 2);
   dchunk = (dchunk / 32) * 32;
   if (dchunk > d.D) dchunk = d.D;
-  const size_t smem = static_cast<size_t>(dchunk) * NT * 8 * 2;
-  cudaError_t e = cudaFuncSetAttribute(route_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  route_kernel<NT><<<route_blocks(d.T), kRouteWarps * 32, smem, s>>>(x, Wg, bias, d.T, d.D, d.E, d.k,
-                                                                     dchunk, ids, w, hist);
+  const size_t stage = static_cast<size_t>(dchunk) * NT * 8 * 2;
+  const size_t reduce = static_cast<size_t>(8) * NT * 4 * 32 * sizeof(float);
+  const size_t smem = stage > reduce ? stage : reduce;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(route_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kRouteSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const int TB = route_block_tokens(d.T);
+  route_kernel<NT><<<route_blocks(d.T), kRouteThreads, smem, s>>>(x, Wg, bias, d.T, d.D, d.E, d.k,
+                                                                  dchunk, TB, ids, w, hist);
   note_launch();
   return cudaGetLastError();
 }
@@ -410,7 +462,7 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* Wg, const float* bia
 }
 
 cudaError_t launch_hist(const int32_t* ids, const moe_dims& d, int32_t* hist, cudaStream_t s) {
-  hist_kernel<<<route_blocks(d.T), 256, 0, s>>>(ids, d.T, d.k, d.E, hist);
+  hist_kernel<<<route_blocks(d.T), 256, 0, s>>>(ids, d.T, d.k, d.E, route_block_tokens(d.T), hist);
   note_launch();
   return cudaGetLastError();
 }
@@ -419,8 +471,9 @@ cudaError_t launch_scatter(const int32_t* ids, const int32_t* hist, const moe_di
                            int32_t* offsets, int32_t* perm, int32_t* inv, const uint16_t* x,
                            uint16_t* x_sorted, cudaStream_t s) {
   const int nblk = route_blocks(d.T);
-  scatter_kernel<<<nblk, kScatterThreads, 0, s>>>(ids, hist, d.T, d.k, d.E, nblk, counts, offsets, perm,
-                                                  inv, reinterpret_cast<const uint4*>(x),
+  scatter_kernel<<<nblk, kScatterThreads, 0, s>>>(ids, hist, d.T, d.k, d.E, route_block_tokens(d.T), nblk,
+                                                  counts, offsets, perm, inv,
+                                                  reinterpret_cast<const uint4*>(x),
                                                   reinterpret_cast<uint4*>(x_sorted), d.D);
   note_launch();
   return cudaGetLastError();

@@ -64,7 +64,7 @@ class Workspace:
         T, D, F, E, k = self.dims
         S = T * k
         rows = S + (T if self.shared else 0)
-        nblk = (T + N.ROUTE_BLOCK_TOKENS - 1) // N.ROUTE_BLOCK_TOKENS
+        nblk = N.route_blocks(T)
         out, off = {}, 0
 
         def take(name, n, dtype, shape):
@@ -147,7 +147,7 @@ def moe_ffn_forward_host(x_host, Wg, W1, W3, W2, k, out_host, workspace: Workspa
 
 def moe_route(x, Wg, k, bias=None):
     """Router GEMM + top-k + softmax -> (ids [T,k] int32, weights [T,k] fp32,
-    block_hist [ceil(T/64), E] int32)."""
+    block_hist [ceil(T/TB), E] int32 with TB = moe_route_block_tokens(T))."""
     T, D = x.shape
     E = Wg.shape[1]
     _need(x, "x", torch.bfloat16, (T, D))
@@ -155,8 +155,7 @@ def moe_route(x, Wg, k, bias=None):
     _need(bias, "bias", torch.float32, (E,))
     ids = torch.empty(T, k, dtype=torch.int32, device=x.device)
     w = torch.empty(T, k, dtype=torch.float32, device=x.device)
-    nblk = (T + N.ROUTE_BLOCK_TOKENS - 1) // N.ROUTE_BLOCK_TOKENS
-    hist = torch.empty(nblk, E, dtype=torch.int32, device=x.device)
+    hist = torch.empty(N.route_blocks(T), E, dtype=torch.int32, device=x.device)
     st = lib.moe_route(_ptr(x), _ptr(Wg), _ptr(bias), N.dims(T, D, 64, E, k), _ptr(ids), _ptr(w),
                        _ptr(hist), _stream())
     check(st, "moe_route")

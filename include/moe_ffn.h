@@ -62,7 +62,6 @@ typedef enum {
 #define MOE_MAX_EXPERTS 128
 #define MOE_MAX_TOPK 16
 #define MOE_MAX_DIM 8192
-#define MOE_ROUTE_BLOCK_TOKENS 64 /* tokens per router/permute block */
 
 /* Layer dimensions: T tokens, D = d_model, F = d_ff, E routed experts, top-k. */
 typedef struct {
@@ -87,7 +86,7 @@ typedef struct {
  * (has_shared != 0 when the shared expert is used; host_io != 0 adds the
  * device staging buffers used by moe_ffn_forward_host).  The workspace holds,
  * each 256-byte aligned: ids [T,k] i32, w [T,k] f32, block histogram
- * [ceil(T/64), E] i32, counts [E] i32, offsets [E+1] i32, perm [T*k] i32,
+ * [ceil(T/TB), E] i32 (TB = moe_route_block_tokens(T)), counts [E] i32, offsets [E+1] i32, perm [T*k] i32,
  * inv [T*k] i32, x_sorted [T*k, D] bf16, h [T*k (+T), F] bf16,
  * y [T*k (+T), D] bf16, then (host_io) x [T, D] and out [T, D] bf16. */
 size_t moe_ffn_workspace_size(moe_dims d, int has_shared, int host_io);
@@ -124,11 +123,16 @@ moe_status moe_ffn_forward_host(const void* x_host, const void* Wg, const float*
 /* Router GEMM + top-k + softmax ("PyTorch MoE implementation": logits, topk,
  * softmax over the selected logits).  ids [T, k] int32, weights [T, k] fp32.
  * block_hist (nullable) receives the per-block expert histogram
- * [ceil(T/64), E] int32 over tokens [64b, 64b+64). */
+ * [ceil(T/TB), E] int32 over tokens [TB b, TB b + TB), TB =
+ * moe_route_block_tokens(T). */
 moe_status moe_route(const void* x, const void* Wg, const float* router_bias, moe_dims d,
                      int32_t* ids, float* weights, int32_t* block_hist, void* stream);
 
-/* Scratch bytes moe_permute needs: the block histogram, ceil(T/64)*E int32. */
+/* Tokens per block of the router and permutation kernels for a batch of T
+ * tokens: 64, or 32 / 16 for batches too small to give every SM two blocks. */
+int moe_route_block_tokens(int T);
+
+/* Scratch bytes moe_permute needs: the block histogram, ceil(T/TB)*E int32. */
 size_t moe_permute_scratch_size(moe_dims d);
 
 /* Stable permutation of the T*k slots by expert id (section "PyTorch MoE
@@ -173,7 +177,8 @@ moe_status moe_combine(const void* y, const float* weights, const int32_t* inv, 
  * callers only.  Arguments and results are those of moe_permute.  The block
  * histogram lives in a fixed 65,536-entry int32 array (256 KB) in the
  * library's own device memory, held on every GPU that loads the library until
- * the process exits; calls with ceil(T/64) * E > 65,536 return
+ * the process exits; calls with ceil(T/TB) * E > 65,536 (TB =
+ * moe_route_block_tokens(T)) return
  * MOE_ERR_UNSUPPORTED_SHAPE.  Every call shares that array: calls whose work
  * overlaps on the GPU race and must be serialised by the caller.  The first
  * call on each device looks up the array's device address (with that device

@@ -21,7 +21,7 @@ def native():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:moe_status|size_t|uint64_t|const char\s*\*)\s*(moe_\w+)\s*\(",
+    return sorted(set(re.findall(r"^\s*(?:moe_status|size_t|uint64_t|int|const char\s*\*)\s*(moe_\w+)\s*\(",
                                  text, flags=re.M)))
 
 
@@ -81,7 +81,8 @@ def test_workspace_size_matches_documented_layout(native):
         a = lambda n: (n + 255) // 256 * 256
         S = T * k
         rows = S + (T if shared else 0)
-        nblk = (T + 63) // 64
+        tb = 64 if T >= 64 * 2 * 152 else 32 if T >= 32 * 2 * 152 else 16
+        nblk = (T + tb - 1) // tb
         n = a(S * 4) * 2 + a(nblk * E * 4) + a(E * 4) + a((E + 1) * 4) + a(S * 4) * 2
         n += a(S * D * 2) + a(rows * F * 2) + a(rows * D * 2)
         if host_io:
@@ -93,6 +94,11 @@ def test_workspace_size_matches_documented_layout(native):
         assert native.lib.moe_ffn_workspace_size(native.dims(T, D, F, E, k), sh, hio) == \
             layout(T, D, F, E, k, sh, hio)
     assert native.lib.moe_ffn_workspace_size(native.dims(10, 100, 64, 4, 2), 0, 0) == 0
+
+
+def test_route_block_tokens(native):
+    assert [native.lib.moe_route_block_tokens(T) for T in (1, 2048, 9727, 9728, 19455, 19456, 32768)] == \
+        [16, 16, 16, 32, 32, 64, 64]
 
 
 def test_product_path_fails_loudly_without_library(tmp_path):

@@ -47,6 +47,8 @@ ROUTE_CASES = [
     (200, 384, 64, 128, 16, False, 5, None),        # widest router, largest k
     (257, 4608, 64, 8, 2, False, 6, None),          # D larger than one staged chunk for E=8? no; long D
     (500, 768, 64, 8, 2, False, 7, inputs.zipf_router_bias(8, 1.2, 7)),
+    (12000, 768, 64, 8, 2, False, 8, None),         # 32-token blocks
+    (20000, 256, 64, 16, 2, False, 9, None),        # 64-token blocks
 ]
 
 
@@ -65,8 +67,11 @@ def test_route(moe, case):
     ok = ~mism
     assert np.abs(w[ok] - w_ref[ok]).max() < 1e-4
     assert np.abs(w.sum(axis=1) - 1).max() < 1e-5
-    for b in range(hist.shape[0]):  # per-64-token-block histogram of the GPU's own ids
-        blk = ids[b * 64:(b + 1) * 64].reshape(-1)
+    from grouped_gemm_router_gb300 import _native
+    tb = int(_native.lib.moe_route_block_tokens(T))
+    assert hist.shape[0] == (T + tb - 1) // tb
+    for b in range(hist.shape[0]):  # per-block histogram of the GPU's own ids
+        blk = ids[b * tb:(b + 1) * tb].reshape(-1)
         assert (hist[b] == np.bincount(blk, minlength=E)).all()
 
 
