@@ -271,12 +271,12 @@ def main():
     T, D, F, E, k = w.T, w.D, w.F, w.E, w.k
     ws = moe.Workspace(T, D, F, E, k, w.shared, device=dev)
     out = torch.empty(T, D, dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
-    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def flush_l2():
-        flush.fill_(1)
-        flush_sink.copy_(flush.sum(dtype=torch.int64))
+        flush.fill_(1.0)
+        flush_sink.copy_(flush.sum())
 
     def step(events=None):
         moe.moe_ffn_forward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], k, bias=G["bias"],
