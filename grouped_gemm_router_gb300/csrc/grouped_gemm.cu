@@ -30,11 +30,11 @@
 // rows of D into that CTA's own TMEM.  Per SM, a 128x256 output tile then
 // stages 16 KB of A and 16 KB of B per 64-deep k-block instead of 16 + 32 KB.
 //
-// Warp roles (320 threads per CTA, one CTA per SM):
+// Warp roles (64 + 32 kEpiWarps threads per CTA, one CTA per SM):
 //   warp 0     TMA producer (one lane) -- both CTAs load their own halves
 //   warp 1     TMEM allocator; MMA issuer (one lane, leader only)
-//   warps 2-9  epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 and the
-//              columns of half (w - 2) / 4 of the tile
+//   warps 2-   epilogue (kEpiWarps): warp w reads TMEM lanes 32 (w % 4) .. + 31
+//              and the columns of part (w - 2) / 4 of the tile
 // Pipelines: kPairStages shared-memory stages (full / empty mbarriers) and
 // two TMEM accumulators of 256 columns (tmem_full / tmem_empty), so the
 // epilogue of one tile overlaps the MMAs of the next.
@@ -57,8 +57,12 @@ namespace moe {
 namespace {
 
 constexpr int kBK = 64;                       // k per stage (128 bytes of bf16)
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
+#ifndef MOE_EPI_WARPS
+#define MOE_EPI_WARPS 8
+#endif
+constexpr int kEpiWarps = MOE_EPI_WARPS;      // epilogue warps per CTA (8 or 16)
+constexpr int kEpiParts = kEpiWarps / 4;      // column parts per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxGroups = MOE_MAX_EXPERTS + 1;
 constexpr uint32_t kTmemCols = 512;           // two 256-column accumulators
 
@@ -89,8 +93,11 @@ constexpr int kPairABytes = 128 * kBK * 2;    // 16 KB: this CTA's 128 rows
 constexpr int kPairBBytesMax = 128 * kBK * 2; // 16 KB: this CTA's half of N <= 256
 constexpr int kPairStageBytes = kPairABytes + kPairBBytesMax;
 constexpr int kOutBoxRows = 32;                 // one epilogue warp's rows
-constexpr int kOutBoxBytes = kOutBoxRows * 128;  // 32 rows x 64 bf16 columns
-constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + kEpiWarps * kOutBoxBytes + 1024;
+constexpr int kOutBoxCols = 32;                 // columns per TMA store box (64 bytes)
+constexpr int kOutBoxBytes = kOutBoxRows * kOutBoxCols * 2;
+constexpr int kOutBufs = kEpiWarps <= 8 ? 2 : 1; // staging buffers per epilogue warp
+constexpr int kPairSmemBytes =
+    kPairStages * kPairStageBytes + kEpiWarps * kOutBufs * kOutBoxBytes + 1024;
 
 struct PairCtl {
   uint64_t full[kPairStages];
@@ -308,18 +315,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ===================== epilogue (both CTAs) =====================
-    // Warp w owns TMEM lanes 32 (w % 4) .. + 31 (32 output rows) and half
-    // (w - 2) / 4 of the tile's columns, in boxes of 64 columns.  A box whose
-    // 32 rows all belong to the group is written through a 128B-swizzled
-    // staging buffer with one TMA store (full 128-byte lines); a box that
-    // crosses the group's end is stored row by row for its valid rows only.
+    // Warp w owns TMEM lanes 32 (w % 4) .. + 31 (32 output rows) and part
+    // (w - 2) / 4 of the tile's columns, in boxes of 32 columns.  A box whose
+    // 32 rows all belong to the group is written through a 64B-swizzled
+    // staging buffer with one TMA store; a box that crosses the group's end is
+    // stored row by row for its valid rows only.
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int part = (warp - 2) >> 2;
     const int r_in_tile = 128 * static_cast<int>(rank) + q * 32 + lane;
     const uint32_t tempty_leader0 = map_to_cta(smem_u32(&ctl.tempty[0]), 0);
     const uint32_t tempty_leader1 = map_to_cta(smem_u32(&ctl.tempty[1]), 0);
-    uint8_t* stage_out = smem + kPairStages * kPairStageBytes + (warp - 2) * kOutBoxBytes;
-    const uint32_t stage_out_u32 = smem_u32(stage_out);
+    uint8_t* stage_out =
+        smem + kPairStages * kPairStageBytes + (warp - 2) * kOutBufs * kOutBoxBytes;
+    int obuf = 0;
     int g = 0;
     int i = 0;
     for (int tile = pair; tile < total; tile += npairs, ++i) {
@@ -339,61 +347,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int col0 = n * hw;
       uint16_t* crow = p.C + static_cast<size_t>(ctl.row0[g] + (valid ? row : 0)) * p.N + col0;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * 256;
-      for (int bc = half * (hw / 2); bc < (half + 1) * (hw / 2); bc += 64) {
-        if (col0 + bc >= p.N) break;  // box past the last column (half-empty last tile)
+      const int cols_per_part = hw / kEpiParts;
+      for (int cc = part * cols_per_part; cc < (part + 1) * cols_per_part; cc += kOutBoxCols) {
+        if (col0 + cc >= p.N) break;  // box past the last column (half-empty last tile)
+        uint32_t packed[16];
+        if (kSwiGLU) {
+          uint32_t rg[32], ru[32];
+          tmem_ld_32cols(taddr + cc, rg);
+          tmem_ld_32cols(taddr + hw + cc, ru);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float g0 = __uint_as_float(rg[2 * j]), g1 = __uint_as_float(rg[2 * j + 1]);
+            const float u0 = __uint_as_float(ru[2 * j]), u1 = __uint_as_float(ru[2 * j + 1]);
+            // silu(g) = g / (1 + exp(-g)); the fast division returns 0 when
+            // exp(-g) overflows, which is the limit of silu for g -> -inf.
+            const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+            const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
+            packed[j] = pack_bf16x2(h0, h1);
+          }
+        } else {
+          uint32_t ra[32];
+          tmem_ld_32cols(taddr + cc, ra);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            packed[j] = pack_bf16x2(__uint_as_float(ra[2 * j]), __uint_as_float(ra[2 * j + 1]));
+        }
         if (full_box) {
-          bulk_wait_group_read0();  // the previous box's store has read the staging buffer
+          // the store issued kOutBufs boxes ago has finished reading this buffer
+          if (kOutBufs == 2)
+            bulk_wait_group_read1();
+          else
+            bulk_wait_group_read0();
           __syncwarp();
-        }
+          uint8_t* sbuf = stage_out + obuf * kOutBoxBytes;
+          // 64B swizzle: 16-byte chunk c of row r lives at chunk c ^ ((r / 2) % 4)
 #pragma unroll
-        for (int cc2 = 0; cc2 < 64; cc2 += 32) {
-          const int cc = bc + cc2;
-          uint32_t packed[16];
-          if (kSwiGLU) {
-            uint32_t rg[32], ru[32];
-            tmem_ld_32cols(taddr + cc, rg);
-            tmem_ld_32cols(taddr + hw + cc, ru);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float g0 = __uint_as_float(rg[2 * j]), g1 = __uint_as_float(rg[2 * j + 1]);
-              const float u0 = __uint_as_float(ru[2 * j]), u1 = __uint_as_float(ru[2 * j + 1]);
-              // silu(g) = g / (1 + exp(-g)); the fast division returns 0 when
-              // exp(-g) overflows, which is the limit of silu for g -> -inf.
-              const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
-              const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
-              packed[j] = pack_bf16x2(h0, h1);
-            }
-          } else {
-            uint32_t ra[32];
-            tmem_ld_32cols(taddr + cc, ra);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              packed[j] = pack_bf16x2(__uint_as_float(ra[2 * j]), __uint_as_float(ra[2 * j + 1]));
+          for (int v = 0; v < 4; ++v) {
+            uint4* dst = reinterpret_cast<uint4*>(sbuf + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4));
+            *dst = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
           }
-          if (full_box) {
-            // 16-byte chunk c of this lane's 128-byte row goes to chunk c ^ (row % 8)
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int chunk = (cc2 >> 3) + v;
-              uint4* dst = reinterpret_cast<uint4*>(stage_out + lane * 128 + ((chunk ^ (lane & 7)) << 4));
-              *dst = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-            }
-          } else if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(crow + cc);
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-          }
-        }
-        if (full_box) {
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&mapC, stage_out_u32, col0 + bc, ctl.row0[g] + warp_row0);
+            tma_store_2d(&mapC, smem_u32(sbuf), col0 + cc, ctl.row0[g] + warp_row0);
             bulk_commit_group();
           }
+          obuf ^= (kOutBufs - 1);
+        } else if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(crow + cc);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
         }
       }
       tc_fence_before_sync();
@@ -431,7 +437,7 @@ cudaError_t get_encoder() {
 }
 
 // 2-D bf16 tensor map of a row-major [rows, cols] matrix, box {box_cols, box_rows},
-// 128-byte swizzle, zero fill outside the tensor.
+// 128-byte swizzle (64-byte for 32-column boxes), zero fill outside the tensor.
 cudaError_t make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
                      uint32_t box_cols) {
   cuuint64_t dims[2] = {cols, rows};
@@ -439,7 +445,8 @@ cudaError_t make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t co
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        box_cols * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -552,7 +559,7 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
   a.shared_a_row0 = 0;
   a.C = h;
   CUtensorMap mC;
-  if ((e = make_map(&mC, h, static_cast<uint64_t>(S) + (shared ? d.T : 0), d.F, kOutBoxRows, 64)) !=
+  if ((e = make_map(&mC, h, static_cast<uint64_t>(S) + (shared ? d.T : 0), d.F, kOutBoxRows, kOutBoxCols)) !=
       cudaSuccess)
     return e;
   e = launch_pair<true>(pair_clusters(true), mA, mAs, mB0, mB1, mB0s, mB1s, mC, a, s);
@@ -591,7 +598,7 @@ cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uin
   a.shared_a_row0 = S;
   a.C = y;
   CUtensorMap mC;
-  if ((e = make_map(&mC, y, hrows, d.D, kOutBoxRows, 64)) != cudaSuccess) return e;
+  if ((e = make_map(&mC, y, hrows, d.D, kOutBoxRows, kOutBoxCols)) != cudaSuccess) return e;
   e = launch_pair<false>(pair_clusters(false), mA, mA, mB0, mB0, mB0s, mB0s, mC, a, s);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
