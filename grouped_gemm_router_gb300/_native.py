@@ -59,6 +59,7 @@ _SIGNATURES = {
     "moe_combine": (_i32, [_vp, _vp, _vp, MoeDims, _i32, _vp, _vp]),
     "moe_permute_noalloc": (_i32, [_vp, MoeDims, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_device_error": (_i32, []),
+    "moe_selftest_wait_timeout": (_i32, [_i32, _vp, _vp]),
     "moe_launch_count": (ctypes.c_uint64, []),
     "moe_status_str": (ctypes.c_char_p, [_i32]),
 }

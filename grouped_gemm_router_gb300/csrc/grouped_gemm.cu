@@ -604,6 +604,30 @@ cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uin
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// Self-test of the bounded waits: one CTA waits on an mbarrier that nothing
+// arrives on; the wait gives up after timeout_ns and records the timeout in
+// the device error word, exactly as a stalled pipeline of the GEMM would.
+__global__ void wait_timeout_selftest_kernel(uint64_t timeout_ns, int* gave_up) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool ok = mbar_wait(smem_u32(&bar), 0, &abort_flag, &g_device_error, timeout_ns);
+    *gave_up = ok ? 0 : 1;
+  }
+}
+
+cudaError_t launch_wait_timeout_selftest(uint64_t timeout_ns, int* gave_up, cudaStream_t s) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(timeout_ns, gave_up);
+  note_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t read_clear_device_error(unsigned int* value) {
   unsigned int zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(value, g_device_error, sizeof(unsigned int));

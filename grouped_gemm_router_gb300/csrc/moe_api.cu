@@ -287,6 +287,12 @@ moe_status moe_device_error(void) {
   return v ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
 }
 
+moe_status moe_selftest_wait_timeout(int timeout_us, int32_t* gave_up, void* stream) {
+  if (timeout_us < 1 || timeout_us > 1000000 || gave_up == nullptr) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_wait_timeout_selftest(static_cast<uint64_t>(timeout_us) * 1000ull, gave_up,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
 uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* moe_status_str(moe_status s) {

@@ -60,18 +60,18 @@ MOE_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with parity `parity` of barrier `bar` to complete.
-// Gives up when *abort is set by another thread or after MOE_WAIT_TIMEOUT_NS;
-// in the second case it sets *abort and the device error word.  Returns
-// false when it gave up.
-MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                       unsigned int* dev_err) {
+// Gives up when *abort is set by another thread or after timeout_ns; in the
+// second case it sets *abort and the device error word.  Returns false when
+// it gave up.
+MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned int* dev_err,
+                       uint64_t timeout_ns = MOE_WAIT_TIMEOUT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > MOE_WAIT_TIMEOUT_NS) {
+      if (global_timer_ns() - t0 > timeout_ns) {
         *abort = 1;
         atomicOr(dev_err, MOE_DEVERR_TIMEOUT);
         return false;

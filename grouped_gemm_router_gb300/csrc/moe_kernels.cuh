@@ -36,6 +36,8 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
 cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uint16_t* Ws2,
                                 const int32_t* offsets, const moe_dims& d, uint16_t* y,
                                 cudaStream_t s);
+// One-CTA kernel whose bounded mbarrier wait must time out (*gave_up = 1).
+cudaError_t launch_wait_timeout_selftest(uint64_t timeout_ns, int* gave_up, cudaStream_t s);
 // Reads and clears the device error word (synchronous).
 cudaError_t read_clear_device_error(unsigned int* value);
 

@@ -194,6 +194,14 @@ moe_status moe_permute_noalloc(const int32_t* ids, moe_dims d, int32_t* counts, 
  * synchronous copy).  Returns MOE_OK or MOE_ERR_DEVICE_TIMEOUT. */
 moe_status moe_device_error(void);
 
+/* Failure-detection self-test: launches one CTA whose bounded mbarrier wait
+ * (the wait every pipelined kernel of the library uses) can never complete;
+ * it gives up after timeout_us (1 .. 10^6 microseconds), writes 1 to
+ * *gave_up (device int32) and records the timeout, so that a following
+ * moe_device_error() returns MOE_ERR_DEVICE_TIMEOUT.  The GPU context stays
+ * usable: nothing faults and nothing is left running. */
+moe_status moe_selftest_wait_timeout(int timeout_us, int32_t* gave_up, void* stream);
+
 /* Number of kernels this library has launched since it was loaded. */
 uint64_t moe_launch_count(void);
 

@@ -73,6 +73,8 @@ def test_argument_validation_before_launch(native):
                                     p(FAKE), None) == N.MOE_ERR_INVALID_ARG     # shared needs x
     assert N.lib.moe_combine(p(FAKE), p(FAKE), p(FAKE), N.dims(4, 96, 64, 4, 2), 0, p(FAKE),
                              None) == N.MOE_ERR_UNSUPPORTED_SHAPE
+    assert N.lib.moe_selftest_wait_timeout(0, p(FAKE), None) == N.MOE_ERR_INVALID_ARG
+    assert N.lib.moe_selftest_wait_timeout(10, None, None) == N.MOE_ERR_INVALID_ARG
     assert N.lib.moe_launch_count() == 0
 
 

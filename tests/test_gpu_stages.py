@@ -228,3 +228,28 @@ def test_grouped_gemms_full_size_sampled(moe, name):
         y_ref = orc.grouped_down(h_got[sel], orc.bf16_to_f64(L["W2"][e:e + 1]), one)
         assert_close(y_got[sel], y_ref, f"y expert {e}", atol=H_ATOL, rtol=H_RTOL)
     assert moe.device_error() == 0
+
+
+def test_bounded_wait_times_out_and_reports(moe):
+    """Failure detection without a GPU fault: a wait on a barrier that nothing
+    signals gives up after its limit, the status is read on the host, and the
+    context stays usable for the next layer call."""
+    from grouped_gemm_router_gb300 import _native as N
+    import ctypes
+    assert moe.device_error() == 0
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = N.lib.moe_selftest_wait_timeout(2000, ctypes.c_void_p(flag.data_ptr()), None)
+    assert st == N.MOE_OK
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 1
+    assert moe.device_error() == N.MOE_ERR_DEVICE_TIMEOUT
+    assert moe.device_error() == 0          # read-and-clear
+    # the context still runs the layer correctly
+    w_, L = _layer(256, 128, 256, 4, 2, False, 10)
+    ids, w, pm, xs_bits = _grouped_inputs(L, 2, 4)
+    h = moe.moe_grouped_swiglu(to_dev(xs_bits), to_dev(pm["offsets"]), to_dev(L["W1"]), to_dev(L["W3"]), 256, 2)
+    torch.cuda.synchronize()
+    h_ref = orc.grouped_swiglu(orc.bf16_to_f64(xs_bits), orc.bf16_to_f64(L["W1"]), orc.bf16_to_f64(L["W3"]),
+                               pm["offsets"])
+    assert_close(to_f64(h), h_ref, "h after a timed-out wait", atol=H_ATOL, rtol=H_RTOL)
+    assert moe.device_error() == 0
