@@ -50,7 +50,8 @@ _SIGNATURES = {
                                ctypes.POINTER(MoeOptions), _vp]),
     "moe_ffn_forward_host": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, MoeDims, _vp, _vp,
                                     _sz, ctypes.POINTER(MoeOptions), _vp]),
-    "moe_route": (_i32, [_vp, _vp, _vp, MoeDims, _vp, _vp, _vp, _vp]),
+    "moe_route_scratch_size": (_sz, [MoeDims]),
+    "moe_route": (_i32, [_vp, _vp, _vp, MoeDims, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_route_block_tokens": (_i32, [_i32]),
     "moe_permute_scratch_size": (_sz, [MoeDims]),
     "moe_permute": (_i32, [_vp, MoeDims, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),

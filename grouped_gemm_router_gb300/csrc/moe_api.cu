@@ -16,6 +16,7 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 struct Workspace {
+  void* wpack;
   int32_t* ids;
   float* w;
   int32_t* hist;
@@ -42,6 +43,7 @@ Workspace carve(void* base, const moe_dims& d, bool shared, bool host_io) {
     off += align_up(bytes);
     return base ? static_cast<char*>(base) + o : nullptr;
   };
+  w.wpack = take(route_packed_bytes(d.D, d.E));
   w.ids = reinterpret_cast<int32_t*>(take(S * 4));
   w.w = reinterpret_cast<float*>(take(S * 4));
   w.hist = reinterpret_cast<int32_t*>(take(static_cast<size_t>(route_blocks(d.T)) * d.E * 4));
@@ -98,7 +100,7 @@ moe_status run_layer(const uint16_t* x, const uint16_t* Wg, const float* bias, c
   if (routed_in)
     e = launch_hist(ids, d, ws.hist, s);
   else
-    e = launch_route(x, Wg, bias, d, ws.ids, ws.w, ws.hist, s);
+    e = launch_route(x, Wg, bias, d, ws.wpack, ws.ids, ws.w, ws.hist, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(o, 1, s);
   e = launch_scatter(ids, ws.hist, d, ws.counts, ws.offsets, ws.perm, ws.inv, x, ws.x_sorted, s);
@@ -195,15 +197,22 @@ moe_status moe_ffn_forward_host(const void* x_host, const void* Wg, const float*
   return MOE_OK;
 }
 
+size_t moe_route_scratch_size(moe_dims d) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return route_packed_bytes(d.D, d.E);
+}
+
 moe_status moe_route(const void* x, const void* Wg, const float* router_bias, moe_dims d,
-                     int32_t* ids, float* weights, int32_t* block_hist, void* stream) {
+                     int32_t* ids, float* weights, int32_t* block_hist, void* scratch,
+                     size_t scratch_bytes, void* stream) {
   moe_status st = check_dims(d);
   if (st != MOE_OK) return st;
-  if (!x || !Wg || !ids || !weights) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(Wg)) return MOE_ERR_INVALID_ARG;
+  if (!x || !Wg || !ids || !weights || !scratch) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wg) || !aligned16(scratch)) return MOE_ERR_INVALID_ARG;
+  if (scratch_bytes < route_packed_bytes(d.D, d.E)) return MOE_ERR_WORKSPACE;
   if (d.T == 0) return MOE_OK;
   return cuda_status(launch_route(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(Wg),
-                                  router_bias, d, ids, weights, block_hist,
+                                  router_bias, d, scratch, ids, weights, block_hist,
                                   static_cast<cudaStream_t>(stream)));
 }
 

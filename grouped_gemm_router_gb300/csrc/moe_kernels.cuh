@@ -14,8 +14,10 @@ void note_launch();
 // ---- routing / permutation (route_permute.cu) ----
 int route_block_tokens(int T);  // tokens per router / permutation block (16, 32 or 64)
 int route_blocks(int T);        // ceil(T / route_block_tokens(T))
+size_t route_packed_bytes(int D, int E);  // router weights in MMA fragment order
+// Packs Wg into wpack_buf (route_packed_bytes bytes), then routes.
 cudaError_t launch_route(const uint16_t* x, const uint16_t* Wg, const float* bias, const moe_dims& d,
-                         int32_t* ids, float* w, int32_t* hist, cudaStream_t s);
+                         void* wpack_buf, int32_t* ids, float* w, int32_t* hist, cudaStream_t s);
 cudaError_t launch_hist(const int32_t* ids, const moe_dims& d, int32_t* hist, cudaStream_t s);
 cudaError_t launch_scatter(const int32_t* ids, const int32_t* hist, const moe_dims& d, int32_t* counts,
                            int32_t* offsets, int32_t* perm, int32_t* inv, const uint16_t* x,

@@ -16,8 +16,7 @@
 
 namespace moe {
 
-constexpr int kRouteThreads = 256;                    // 8 warps per router block
-constexpr int kRouteSmemBytes = 64 * 1024;            // staged router weights per D-chunk
+constexpr int kRouteThreads = 256;  // 8 warps per router block
 
 // Tokens per router / permutation block: 64 when that still gives every SM two
 // blocks, else 32 or 16, so that small batches spread over the whole GPU.
@@ -32,6 +31,16 @@ int route_blocks(int T) {
   return (T + tb - 1) / tb;
 }
 
+// Expert tiles of 8 (the MMA's N) for E experts, padded to the instantiated widths.
+int route_expert_tiles(int E) {
+  const int nt = (E + 7) / 8;
+  return nt <= 2 ? nt : nt <= 4 ? 4 : nt <= 8 ? 8 : 16;
+}
+
+size_t route_packed_bytes(int D, int E) {
+  return static_cast<size_t>(D / 32) * route_expert_tiles(E) * 32 * 16;
+}
+
 MOE_DEV void mma_m16n8k16_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -41,33 +50,47 @@ MOE_DEV void mma_m16n8k16_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Block = 8 warps for TB = 16 MT tokens (MT = 1, 2 or 4 tiles of 16 tokens).
-// Warp w computes tile w % MT over the 32-wide D-chunks kc with
-// kc % DS == w / MT (DS = 8 / MT warps share a tile); their partial logits are
-// summed through shared memory before the selection.  Lane
-// (g = lane / 4, c = lane % 4) loads 16 bytes of rows g and g + 8 at columns
-// d + 8c .. d + 8c + 7 of a 32-wide chunk: a coalesced 64-byte segment per
-// row.  The reduction order over d inside a chunk is irrelevant, so those 8
-// columns feed two m16n8k16 MMAs as their (2c, 2c+1, 2c+8, 2c+9) columns, and
-// the router weights are staged in shared memory in the matching order:
-// wpack[chunk][expert tile][lane] = Wg[32 chunk + 8c + 0..7][8 tile + g].
-//
-// Selection: thread (g, c) holds the logits of experts 8n + 2c + {0,1} for
-// rows g and g + 8.  Each of the k rounds takes the largest not-yet-chosen
-// logit (ties to the lower expert index) across the quad.
+// The router's x loads put, for lane (g = lane / 4, c = lane % 4), columns
+// d + 8c .. d + 8c + 7 of each 32-wide chunk into the MMA k-slots (2c, 2c+1,
+// 2c+8, 2c+9) of two m16n8k16 MMAs; the order of terms in the sum over d is
+// irrelevant.  The router weights are packed once per call in the matching
+// fragment order: wpack[chunk][expert tile][lane] = 16 bytes holding
+// Wg[32 chunk + 8c + j][8 tile + g], j = 0..7 (zero for padded experts).
+__global__ void __launch_bounds__(256) pack_router_weights_kernel(const uint16_t* __restrict__ Wg, int D,
+                                                                  int E, int NT, uint4* __restrict__ wpack) {
+  const int slot = blockIdx.x * blockDim.x + threadIdx.x;
+  if (slot >= (D / 32) * NT * 32) return;
+  const int lane = slot & 31, n = (slot >> 5) % NT, kc = (slot >> 5) / NT;
+  const int e = 8 * n + (lane >> 2), d0 = 32 * kc + 8 * (lane & 3);
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t lo = e < E ? Wg[static_cast<size_t>(d0 + 2 * j) * E + e] : 0u;
+    const uint32_t hi = e < E ? Wg[static_cast<size_t>(d0 + 2 * j + 1) * E + e] : 0u;
+    w[j] = lo | (hi << 16);
+  }
+  wpack[slot] = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // Resident blocks per SM the register budget is sized for: all blocks of a
 // 32K-token batch (512 blocks) fit in one wave for E <= 8.
-constexpr int route_min_blocks(int nt) { return nt <= 1 ? 4 : nt <= 2 ? 3 : nt <= 8 ? 2 : 1; }
+constexpr int route_min_blocks(int nt) { return nt <= 1 ? 3 : nt <= 2 ? 3 : nt <= 8 ? 2 : 1; }
 
-template <int NT>
+// Block = 8 warps for TB = 16 MT tokens (MT = 1, 2 or 4 tiles of 16 tokens).
+// Warp w computes tile w % MT over the 32-wide D-chunks kc with
+// kc % DS == w / MT (DS = 8 / MT warps share a tile), loading x and the packed
+// weight fragments straight from memory in batches of KG chunks; the DS
+// partial results of a tile are summed through shared memory.
+//
+// Selection: thread (g, c) holds the logits of experts 8n + 2c + {0,1} for
+// rows g and g + 8.  Each of the k rounds (k <= KMAX) takes the largest
+// not-yet-chosen logit (ties to the lower expert index) across the quad.
+template <int NT, int KMAX>
 __global__ void __launch_bounds__(kRouteThreads, route_min_blocks(NT)) route_kernel(
-    const uint16_t* __restrict__ x, const uint16_t* __restrict__ Wg, const float* __restrict__ bias,
-    int T, int D, int E, int k, int dchunk, int TB, int32_t* __restrict__ ids,
-    float* __restrict__ wts, int32_t* __restrict__ hist) {
-  extern __shared__ __align__(16) uint8_t route_smem[];
-  uint4* wpack = reinterpret_cast<uint4*>(route_smem);
-  uint16_t* wpack16 = reinterpret_cast<uint16_t*>(route_smem);
-  float* red = reinterpret_cast<float*>(route_smem);  // reused after the D loop
+    const uint16_t* __restrict__ x, const uint4* __restrict__ wpack, const float* __restrict__ bias,
+    int T, int D, int E, int k, int TB, int32_t* __restrict__ ids, float* __restrict__ wts,
+    int32_t* __restrict__ hist) {
+  extern __shared__ float red[];  // [8 warps][NT][4][32]: partial logits
   __shared__ int s_hist[MOE_MAX_EXPERTS];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -86,75 +109,33 @@ __global__ void __launch_bounds__(kRouteThreads, route_min_blocks(NT)) route_ker
 #pragma unroll
   for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 
-  constexpr int EP = NT * 8;                            // experts padded to whole MMA tiles
-  constexpr int KG = (NT >= 8) ? 2 : 4;      // chunks per load batch
-  for (int d0 = 0; d0 < D; d0 += dchunk) {
-    const int dc = min(dchunk, D - d0);
-    __syncthreads();
-    // Stage Wg[d0 : d0 + dc, :] (dc * E contiguous bf16, a multiple of 8) in
-    // fragment order, 16-byte loads issued in batches; padded experts are 0.
-    if (E < EP) {
-      const int nz = dc * EP / 8;
-      for (int i = threadIdx.x; i < nz; i += blockDim.x) wpack[i] = make_uint4(0, 0, 0, 0);
-      __syncthreads();
+  constexpr int KG = (NT >= 16) ? 1 : (NT >= 8) ? 2 : 4;  // chunks per load batch
+  const int nkc = D >> 5;
+  for (int kc0 = split; kc0 < nkc; kc0 += KG * DS) {
+    // all loads of the batch first: x (2 rows x KG chunks) and the weights
+    uint4 a0[KG], a1[KG], b[KG][NT];
+#pragma unroll
+    for (int j = 0; j < KG; ++j) {
+      const int kc = kc0 + j * DS;
+      const bool in = kc < nkc;
+      const int q = (kc << 2) + c;  // 16-byte column index
+      a0[j] = (ok0 && in) ? __ldg(xr0 + q) : make_uint4(0, 0, 0, 0);
+      a1[j] = (ok1 && in) ? __ldg(xr1 + q) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+        b[j][n] = in ? __ldg(wpack + (static_cast<size_t>(kc) * NT + n) * 32 + lane) : make_uint4(0, 0, 0, 0);
     }
-    const uint4* src = reinterpret_cast<const uint4*>(Wg + static_cast<size_t>(d0) * E);
-    const int nvec = dc * E / 8;
-    for (int base = threadIdx.x; base < nvec; base += blockDim.x * 4) {
-      uint4 v[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int idx = base + j * blockDim.x;
-        v[j] = idx < nvec ? __ldg(src + idx) : make_uint4(0, 0, 0, 0);
-      }
+    for (int j = 0; j < KG; ++j) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int idx = base + j * blockDim.x;
-        if (idx >= nvec) continue;
-        const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-        int dd = (idx * 8) / E, e = idx * 8 - dd * E;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const uint16_t val = static_cast<uint16_t>((t & 1) ? (w4[t >> 1] >> 16) : (w4[t >> 1] & 0xFFFFu));
-          const int kc = dd >> 5, r = dd & 31;
-          const int ln = (e & 7) * 4 + (r >> 3);
-          wpack16[((static_cast<size_t>(kc) * NT + (e >> 3)) * 32 + ln) * 8 + (r & 7)] = val;
-          if (++e == E) {
-            e = 0;
-            ++dd;
-          }
-        }
-      }
-    }
-    __syncthreads();
-    const int nkc = dc >> 5;
-    for (int kc0 = split; kc0 < nkc; kc0 += KG * DS) {
-      // all x loads of the batch first (2 rows x KG chunks of 16 bytes)
-      uint4 a0[KG], a1[KG];
-#pragma unroll
-      for (int j = 0; j < KG; ++j) {
-        const int kc = kc0 + j * DS;
-        const int q = ((d0 + kc * 32) >> 3) + c;  // 16-byte column index
-        const bool in = kc < nkc;
-        a0[j] = (ok0 && in) ? __ldg(xr0 + q) : make_uint4(0, 0, 0, 0);
-        a1[j] = (ok1 && in) ? __ldg(xr1 + q) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int j = 0; j < KG; ++j) {
-        const int kc = kc0 + j * DS;
-        if (kc >= nkc) break;
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          const uint4 b = wpack[(static_cast<size_t>(kc) * NT + n) * 32 + lane];
-          mma_m16n8k16_bf16(acc[n], a0[j].x, a1[j].x, a0[j].y, a1[j].y, b.x, b.y);
-          mma_m16n8k16_bf16(acc[n], a0[j].z, a1[j].z, a0[j].w, a1[j].w, b.z, b.w);
-        }
+      for (int n = 0; n < NT; ++n) {
+        mma_m16n8k16_bf16(acc[n], a0[j].x, a1[j].x, a0[j].y, a1[j].y, b[j][n].x, b[j][n].y);
+        mma_m16n8k16_bf16(acc[n], a0[j].z, a1[j].z, a0[j].w, a1[j].w, b[j][n].z, b[j][n].w);
       }
     }
   }
 
-  // ---- sum the DS partial results of each tile (shared memory reused) ----
-  __syncthreads();
+  // ---- sum the DS partial results of each tile ----
   if (split > 0) {
 #pragma unroll
     for (int n = 0; n < NT; ++n)
@@ -188,10 +169,10 @@ __global__ void __launch_bounds__(kRouteThreads, route_min_blocks(NT)) route_ker
       }
     }
     uint32_t taken = 0;
-    float sel_v[MOE_MAX_TOPK];
-    int sel_e[MOE_MAX_TOPK];
+    float sel_v[KMAX];
+    int sel_e[KMAX];
 #pragma unroll
-    for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+    for (int j = 0; j < KMAX; ++j) {
       sel_v[j] = 0.f;
       sel_e[j] = 0;
       if (j < k) {
@@ -223,10 +204,10 @@ __global__ void __launch_bounds__(kRouteThreads, route_min_blocks(NT)) route_ker
         sel_e[j] = be;
       }
     }
-    float z[MOE_MAX_TOPK];
+    float z[KMAX];
     float sum = 0.f;
 #pragma unroll
-    for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+    for (int j = 0; j < KMAX; ++j) {
       z[j] = 0.f;
       if (j < k) {
         z[j] = expf(sel_v[j] - sel_v[0]);
@@ -235,7 +216,7 @@ __global__ void __launch_bounds__(kRouteThreads, route_min_blocks(NT)) route_ker
     }
     if (row < T) {
 #pragma unroll
-      for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+      for (int j = 0; j < KMAX; ++j) {
         if (j < k && (j & 3) == c) {
           ids[static_cast<size_t>(row) * k + j] = sel_e[j];
           wts[static_cast<size_t>(row) * k + j] = z[j] / sum;
@@ -418,46 +399,55 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
   }
 }
 
-template <int NT>
-static cudaError_t launch_route_nt(const uint16_t* x, const uint16_t* Wg, const float* bias,
+template <int NT, int KMAX>
+static cudaError_t launch_route_nt(const uint16_t* x, const uint4* wpack, const float* bias,
                                   const moe_dims& d, int32_t* ids, float* w, int32_t* hist,
                                   cudaStream_t s) {
-  int dchunk = kRouteSmemBytes / (NT * 8 * 2);
-  dchunk = (dchunk / 32) * 32;
-  if (dchunk > d.D) dchunk = d.D;
-  const size_t stage = static_cast<size_t>(dchunk) * NT * 8 * 2;
-  const size_t reduce = static_cast<size_t>(8) * NT * 4 * 32 * sizeof(float);
-  const size_t smem = stage > reduce ? stage : reduce;
-  static bool attr_done[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(route_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kRouteSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
   const int TB = route_block_tokens(d.T);
-  route_kernel<NT><<<route_blocks(d.T), kRouteThreads, smem, s>>>(x, Wg, bias, d.T, d.D, d.E, d.k,
-                                                                  dchunk, TB, ids, w, hist);
+  constexpr size_t smem = static_cast<size_t>(8) * NT * 4 * 32 * sizeof(float);
+  if (smem > 48 * 1024) {
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_done[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(route_kernel<NT, KMAX>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      attr_done[dev] = true;
+    }
+  }
+  route_kernel<NT, KMAX><<<route_blocks(d.T), kRouteThreads, smem, s>>>(x, wpack, bias, d.T, d.D, d.E,
+                                                                        d.k, TB, ids, w, hist);
   note_launch();
   return cudaGetLastError();
 }
 
+template <int NT>
+static cudaError_t launch_route_k(const uint16_t* x, const uint4* wpack, const float* bias,
+                                 const moe_dims& d, int32_t* ids, float* w, int32_t* hist,
+                                 cudaStream_t s) {
+  if (d.k <= 2) return launch_route_nt<NT, 2>(x, wpack, bias, d, ids, w, hist, s);
+  if (d.k <= 4) return launch_route_nt<NT, 4>(x, wpack, bias, d, ids, w, hist, s);
+  if (d.k <= 8) return launch_route_nt<NT, 8>(x, wpack, bias, d, ids, w, hist, s);
+  return launch_route_nt<NT, 16>(x, wpack, bias, d, ids, w, hist, s);
+}
+
 cudaError_t launch_route(const uint16_t* x, const uint16_t* Wg, const float* bias, const moe_dims& d,
-                         int32_t* ids, float* w, int32_t* hist, cudaStream_t s) {
-  const int nt = (d.E + 7) / 8;
-  switch (nt) {
-    case 1: return launch_route_nt<1>(x, Wg, bias, d, ids, w, hist, s);
-    case 2: return launch_route_nt<2>(x, Wg, bias, d, ids, w, hist, s);
-    case 3:
-    case 4: return launch_route_nt<4>(x, Wg, bias, d, ids, w, hist, s);
-    case 5:
-    case 6:
-    case 7:
-    case 8: return launch_route_nt<8>(x, Wg, bias, d, ids, w, hist, s);
-    default: return launch_route_nt<16>(x, Wg, bias, d, ids, w, hist, s);
+                         void* wpack_buf, int32_t* ids, float* w, int32_t* hist, cudaStream_t s) {
+  const int NT = route_expert_tiles(d.E);
+  uint4* wpack = static_cast<uint4*>(wpack_buf);
+  const int nslots = (d.D / 32) * NT * 32;
+  pack_router_weights_kernel<<<(nslots + 255) / 256, 256, 0, s>>>(Wg, d.D, d.E, NT, wpack);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  switch (NT) {
+    case 1: return launch_route_k<1>(x, wpack, bias, d, ids, w, hist, s);
+    case 2: return launch_route_k<2>(x, wpack, bias, d, ids, w, hist, s);
+    case 4: return launch_route_k<4>(x, wpack, bias, d, ids, w, hist, s);
+    case 8: return launch_route_k<8>(x, wpack, bias, d, ids, w, hist, s);
+    default: return launch_route_k<16>(x, wpack, bias, d, ids, w, hist, s);
   }
 }
 

@@ -73,6 +73,8 @@ class Workspace:
             out[name] = self.buf[off:off + size].view(dtype).view(*shape)
             off += (size + 255) // 256 * 256
 
+        npack = int(lib.moe_route_scratch_size(N.dims(T, D, F, E, k)))
+        take("router_packed", npack, torch.uint8, (npack,))
         take("ids", S, torch.int32, (T, k))
         take("w", S, torch.float32, (T, k))
         take("hist", nblk * E, torch.int32, (nblk, E))
@@ -156,8 +158,11 @@ def moe_route(x, Wg, k, bias=None):
     ids = torch.empty(T, k, dtype=torch.int32, device=x.device)
     w = torch.empty(T, k, dtype=torch.float32, device=x.device)
     hist = torch.empty(N.route_blocks(T), E, dtype=torch.int32, device=x.device)
-    st = lib.moe_route(_ptr(x), _ptr(Wg), _ptr(bias), N.dims(T, D, 64, E, k), _ptr(ids), _ptr(w),
-                       _ptr(hist), _stream())
+    d = N.dims(T, D, 64, E, k)
+    nscratch = int(lib.moe_route_scratch_size(d))
+    scratch = torch.empty(max(nscratch, 16), dtype=torch.uint8, device=x.device)
+    st = lib.moe_route(_ptr(x), _ptr(Wg), _ptr(bias), d, _ptr(ids), _ptr(w), _ptr(hist), _ptr(scratch),
+                       nscratch, _stream())
     check(st, "moe_route")
     return ids, w, hist
 

@@ -85,7 +85,8 @@ typedef struct {
 /* Bytes of device workspace moe_ffn_forward needs for these dimensions
  * (has_shared != 0 when the shared expert is used; host_io != 0 adds the
  * device staging buffers used by moe_ffn_forward_host).  The workspace holds,
- * each 256-byte aligned: ids [T,k] i32, w [T,k] f32, block histogram
+ * each 256-byte aligned: the packed router weights (moe_route_scratch_size
+ * bytes), ids [T,k] i32, w [T,k] f32, block histogram
  * [ceil(T/TB), E] i32 (TB = moe_route_block_tokens(T)), counts [E] i32, offsets [E+1] i32, perm [T*k] i32,
  * inv [T*k] i32, x_sorted [T*k, D] bf16, h [T*k (+T), F] bf16,
  * y [T*k (+T), D] bf16, then (host_io) x [T, D] and out [T, D] bf16. */
@@ -120,13 +121,19 @@ moe_status moe_ffn_forward_host(const void* x_host, const void* Wg, const float*
 
 /* ---- Stage entry points (the same kernels moe_ffn_forward launches) ---- */
 
+/* Scratch bytes moe_route needs: the router weights repacked in the MMA
+ * fragment order, (D/32) * (E rounded up to 8, 16, 32, 64 or 128) * 16 bytes. */
+size_t moe_route_scratch_size(moe_dims d);
+
 /* Router GEMM + top-k + softmax ("PyTorch MoE implementation": logits, topk,
  * softmax over the selected logits).  ids [T, k] int32, weights [T, k] fp32.
  * block_hist (nullable) receives the per-block expert histogram
  * [ceil(T/TB), E] int32 over tokens [TB b, TB b + TB), TB =
- * moe_route_block_tokens(T). */
+ * moe_route_block_tokens(T).  scratch (device, 16-byte aligned) holds
+ * moe_route_scratch_size(d) bytes. */
 moe_status moe_route(const void* x, const void* Wg, const float* router_bias, moe_dims d,
-                     int32_t* ids, float* weights, int32_t* block_hist, void* stream);
+                     int32_t* ids, float* weights, int32_t* block_hist, void* scratch,
+                     size_t scratch_bytes, void* stream);
 
 /* Tokens per block of the router and permutation kernels for a batch of T
  * tokens: 64, or 32 / 16 for batches too small to give every SM two blocks. */

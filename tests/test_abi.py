@@ -64,7 +64,11 @@ def test_argument_validation_before_launch(native):
     assert _forward(N, good, shared=(FAKE, None, FAKE)) == N.MOE_ERR_INVALID_ARG   # partial shared
     assert _forward(N, good, ws_bytes=100) == N.MOE_ERR_WORKSPACE
     p = ctypes.c_void_p
-    assert N.lib.moe_route(None, p(FAKE), None, good, p(FAKE), p(FAKE), None, None) == N.MOE_ERR_INVALID_ARG
+    assert N.lib.moe_route(None, p(FAKE), None, good, p(FAKE), p(FAKE), None, p(FAKE), 1 << 20,
+                           None) == N.MOE_ERR_INVALID_ARG
+    assert N.lib.moe_route(p(FAKE), p(FAKE), None, good, p(FAKE), p(FAKE), None, p(FAKE), 16,
+                           None) == N.MOE_ERR_WORKSPACE
+    assert N.lib.moe_route_scratch_size(N.dims(10, 768, 64, 64, 4)) == 24 * 8 * 32 * 16
     assert N.lib.moe_permute(p(FAKE), good, p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), None,
                              p(FAKE), 1 << 20, None) == N.MOE_ERR_INVALID_ARG   # x without x_sorted
     assert N.lib.moe_permute(p(FAKE), good, p(FAKE), p(FAKE), p(FAKE), p(FAKE), None, None,
@@ -85,7 +89,9 @@ def test_workspace_size_matches_documented_layout(native):
         rows = S + (T if shared else 0)
         tb = 64 if T >= 64 * 2 * 152 else 32 if T >= 32 * 2 * 152 else 16
         nblk = (T + tb - 1) // tb
-        n = a(S * 4) * 2 + a(nblk * E * 4) + a(E * 4) + a((E + 1) * 4) + a(S * 4) * 2
+        et = (E + 7) // 8
+        et = et if et <= 2 else 4 if et <= 4 else 8 if et <= 8 else 16
+        n = a((D // 32) * et * 32 * 16) + a(S * 4) * 2 + a(nblk * E * 4) + a(E * 4) + a((E + 1) * 4) + a(S * 4) * 2
         n += a(S * D * 2) + a(rows * F * 2) + a(rows * D * 2)
         if host_io:
             n += 2 * a(T * D * 2)
