@@ -34,6 +34,8 @@ template <int KMAX, int U>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const uint4* __restrict__ y, const float* __restrict__ w, const int32_t* __restrict__ inv, int T,
     int D, int k, int S, int has_shared, uint4* __restrict__ out) {
+  griddep_wait();  // y comes from the previous kernel
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kCombineWarps + warp;
   if (t >= T) return;
@@ -94,28 +96,21 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
 }
 
 template <int KMAX, int U>
-static void launch_combine_k(const uint16_t* y, const float* w, const int32_t* inv, const moe_dims& d,
-                             int has_shared, uint16_t* out, cudaStream_t s) {
+static cudaError_t launch_combine_k(const uint16_t* y, const float* w, const int32_t* inv, const moe_dims& d,
+                                    int has_shared, uint16_t* out, cudaStream_t s, bool pdl) {
   const int grid = (d.T + kCombineWarps - 1) / kCombineWarps;
-  combine_kernel<KMAX, U><<<grid, kCombineThreads, 0, s>>>(
-      reinterpret_cast<const uint4*>(y), w, inv, d.T, d.D, d.k, d.T * d.k, has_shared,
-      reinterpret_cast<uint4*>(out));
+  return launch_kernel(combine_kernel<KMAX, U>, dim3(grid), dim3(kCombineThreads), 0, s, pdl,
+                       reinterpret_cast<const uint4*>(y), w, inv, d.T, d.D, d.k, d.T * d.k, has_shared,
+                       reinterpret_cast<uint4*>(out));
 }
 
 cudaError_t launch_combine(const uint16_t* y, const float* w, const int32_t* inv, const moe_dims& d,
-                           int has_shared, uint16_t* out, cudaStream_t s) {
-  if (d.k <= 1)
-    launch_combine_k<1, 4>(y, w, inv, d, has_shared, out, s);
-  else if (d.k <= 2)
-    launch_combine_k<2, 3>(y, w, inv, d, has_shared, out, s);
-  else if (d.k <= 4)
-    launch_combine_k<4, 2>(y, w, inv, d, has_shared, out, s);
-  else if (d.k <= 8)
-    launch_combine_k<8, 1>(y, w, inv, d, has_shared, out, s);
-  else
-    launch_combine_k<16, 1>(y, w, inv, d, has_shared, out, s);
-  note_launch();
-  return cudaGetLastError();
+                           int has_shared, uint16_t* out, cudaStream_t s, bool pdl) {
+  if (d.k <= 1) return launch_combine_k<1, 4>(y, w, inv, d, has_shared, out, s, pdl);
+  if (d.k <= 2) return launch_combine_k<2, 3>(y, w, inv, d, has_shared, out, s, pdl);
+  if (d.k <= 4) return launch_combine_k<4, 2>(y, w, inv, d, has_shared, out, s, pdl);
+  if (d.k <= 8) return launch_combine_k<8, 1>(y, w, inv, d, has_shared, out, s, pdl);
+  return launch_combine_k<16, 1>(y, w, inv, d, has_shared, out, s, pdl);
 }
 
 }  // namespace moe

@@ -139,6 +139,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkb = p.K / kBK;
   const int half_n = p.tile_n / 2;                    // B columns staged by this CTA
 
+  // ---- setup that reads nothing produced by earlier kernels ----
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapB0);
+    if (kSwiGLU) tma_prefetch_desc(&mapB1);
+    for (int st = 0; st < kPairStages; ++st) {
+      mbar_init(smem_u32(&ctl.full[st]), 1);
+      mbar_init(smem_u32(&ctl.empty[st]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ctl.tfull[b]), 1);
+      mbar_init(smem_u32(&ctl.tempty[b]), 2 * kEpiWarps);
+    }
+    mbar_init(smem_u32(&ctl.drain), 1);
+    ctl.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&ctl.tmem_base), kTmemCols);
+    tmem_relinquish_pair();
+    tc_fence_before_sync();
+  }
+  griddep_launch_dependents();
+  griddep_wait();  // offsets and the A operand come from earlier kernels
+
   // ---- group table and tile prefix (identical in both CTAs) ----
   for (int g = threadIdx.x; g < G; g += kThreads) {
     if (g < p.E) {
@@ -176,26 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ctl.tile_prefix[G] = incl;
       ctl.total_tiles = incl;
     }
-    if (lane == 0) {
-      for (int st = 0; st < kPairStages; ++st) {
-        mbar_init(smem_u32(&ctl.full[st]), 1);
-        mbar_init(smem_u32(&ctl.empty[st]), 1);
-      }
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(smem_u32(&ctl.tfull[b]), 1);
-        mbar_init(smem_u32(&ctl.tempty[b]), 2 * kEpiWarps);
-      }
-      mbar_init(smem_u32(&ctl.drain), 1);
-      ctl.abort = 0;
-      fence_mbar_init();
-    }
   }
-  if (warp == 1) {
-    tmem_alloc_pair(smem_u32(&ctl.tmem_base), kTmemCols);
-    tmem_relinquish_pair();
-    tc_fence_before_sync();
-  }
-  // barrier inits and TMEM allocation visible to both CTAs before any use
+  // barrier inits, the tile table and the TMEM allocation visible to both CTAs
   cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl.tmem_base;
@@ -206,9 +213,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ===================== TMA producer (both CTAs) =====================
     if (lane == 0) {
-      tma_prefetch_desc(&mapA);
-      tma_prefetch_desc(&mapB0);
-      if (kSwiGLU) tma_prefetch_desc(&mapB1);
       const uint64_t pol_a = l2_policy_evict_normal();
       const uint64_t pol_b = l2_policy_evict_last();
       const uint32_t pair_tx = 2u * static_cast<uint32_t>(kPairABytes + half_n * kBK * 2);
@@ -463,19 +467,21 @@ template <bool kSwiGLU>
 cudaError_t launch_pair(int nclusters, const CUtensorMap& a, const CUtensorMap& as,
                         const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b0s,
                         const CUtensorMap& b1s, const CUtensorMap& c, const GemmArgs& args,
-                        cudaStream_t s) {
+                        cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * nclusters, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kPairSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kSwiGLU>, a, as, b0, b1, b0s, b1s, c, args);
 }
 
@@ -527,7 +533,7 @@ int pair_clusters(bool swiglu) {
 cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, const uint16_t* W1,
                                   const uint16_t* W3, const uint16_t* Ws1, const uint16_t* Ws3,
                                   const int32_t* offsets, const moe_dims& d, uint16_t* h,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, bool pdl) {
   cudaError_t e = get_encoder();
   if (e != cudaSuccess) return e;
   int sms = 0;
@@ -562,14 +568,14 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
   if ((e = make_map(&mC, h, static_cast<uint64_t>(S) + (shared ? d.T : 0), d.F, kOutBoxRows, kOutBoxCols)) !=
       cudaSuccess)
     return e;
-  e = launch_pair<true>(pair_clusters(true), mA, mAs, mB0, mB1, mB0s, mB1s, mC, a, s);
+  e = launch_pair<true>(pair_clusters(true), mA, mAs, mB0, mB1, mB0s, mB1s, mC, a, s, pdl);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uint16_t* Ws2,
                                 const int32_t* offsets, const moe_dims& d, uint16_t* y,
-                                cudaStream_t s) {
+                                cudaStream_t s, bool pdl) {
   cudaError_t e = get_encoder();
   if (e != cudaSuccess) return e;
   int sms = 0;
@@ -599,7 +605,7 @@ cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uin
   a.C = y;
   CUtensorMap mC;
   if ((e = make_map(&mC, y, hrows, d.D, kOutBoxRows, kOutBoxCols)) != cudaSuccess) return e;
-  e = launch_pair<false>(pair_clusters(false), mA, mA, mB0, mB0, mB0s, mB0s, mC, a, s);
+  e = launch_pair<false>(pair_clusters(false), mA, mA, mB0, mB0, mB0s, mB0s, mC, a, s, pdl);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -96,23 +96,27 @@ moe_status run_layer(const uint16_t* x, const uint16_t* Wg, const float* bias, c
   const int32_t* ids = routed_in ? o->ids_in : ws.ids;
   const float* w = routed_in ? o->weights_in : ws.w;
   cudaError_t e;
+  // Every kernel after the first may start while its predecessor finishes
+  // (programmatic dependent launch): it waits on the device before reading
+  // the predecessor's results.  Stage events between kernels, when given,
+  // serialise the launches again.
   record(o, 0, s);
   if (routed_in)
-    e = launch_hist(ids, d, ws.hist, s);
+    e = launch_hist(ids, d, ws.hist, s, false);
   else
-    e = launch_route(x, Wg, bias, d, ws.wpack, ws.ids, ws.w, ws.hist, s);
+    e = launch_route(x, Wg, bias, d, ws.wpack, ws.ids, ws.w, ws.hist, s, false);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(o, 1, s);
-  e = launch_scatter(ids, ws.hist, d, ws.counts, ws.offsets, ws.perm, ws.inv, x, ws.x_sorted, s);
+  e = launch_scatter(ids, ws.hist, d, ws.counts, ws.offsets, ws.perm, ws.inv, x, ws.x_sorted, s, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(o, 2, s);
-  e = launch_grouped_swiglu(ws.x_sorted, x, W1, W3, Ws1, Ws3, ws.offsets, d, ws.h, s);
+  e = launch_grouped_swiglu(ws.x_sorted, x, W1, W3, Ws1, Ws3, ws.offsets, d, ws.h, s, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(o, 3, s);
-  e = launch_grouped_down(ws.h, W2, Ws2, ws.offsets, d, ws.y, s);
+  e = launch_grouped_down(ws.h, W2, Ws2, ws.offsets, d, ws.y, s, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(o, 4, s);
-  e = launch_combine(ws.y, w, ws.inv, d, shared ? 1 : 0, out, s);
+  e = launch_combine(ws.y, w, ws.inv, d, shared ? 1 : 0, out, s, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(o, 5, s);
   return MOE_OK;

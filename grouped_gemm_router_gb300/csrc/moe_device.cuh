@@ -369,6 +369,15 @@ MOE_DEV float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
 MOE_DEV uint32_t lane_id() { return threadIdx.x & 31u; }
 
+// Programmatic dependent launch: wait until the preceding kernel of the
+// stream has completed and its writes are visible (returns at once when this
+// kernel was not launched as a programmatic dependent) ...
+MOE_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// ... and allow the next kernel of the stream to start launching now.
+MOE_DEV void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 MOE_DEV bool elect_one_sync() {
   uint32_t pred = 0;
   asm volatile(

@@ -58,6 +58,7 @@ MOE_DEV void mma_m16n8k16_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t
 // Wg[32 chunk + 8c + j][8 tile + g], j = 0..7 (zero for padded experts).
 __global__ void __launch_bounds__(256) pack_router_weights_kernel(const uint16_t* __restrict__ Wg, int D,
                                                                   int E, int NT, uint4* __restrict__ wpack) {
+  griddep_launch_dependents();
   const int slot = blockIdx.x * blockDim.x + threadIdx.x;
   if (slot >= (D / 32) * NT * 32) return;
   const int lane = slot & 31, n = (slot >> 5) % NT, kc = (slot >> 5) / NT;
@@ -93,6 +94,8 @@ __global__ void __launch_bounds__(kRouteThreads, route_min_blocks(NT)) route_ker
   extern __shared__ float red[];  // [8 warps][NT][4][32]: partial logits
   __shared__ int s_hist[MOE_MAX_EXPERTS];
 
+  griddep_wait();  // packed weights (and, in a layer, nothing else) come from the previous kernel
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int MT = TB >> 4, DS = 8 / MT;
@@ -236,6 +239,8 @@ __global__ void __launch_bounds__(kRouteThreads, route_min_blocks(NT)) route_ker
 __global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ ids, int T, int k,
                                                    int E, int TB, int32_t* __restrict__ hist) {
   __shared__ int s_hist[MOE_MAX_EXPERTS];
+  griddep_wait();
+  griddep_launch_dependents();
   for (int i = threadIdx.x; i < E; i += blockDim.x) s_hist[i] = 0;
   __syncthreads();
   const int s0 = blockIdx.x * TB * k;  // T * k <= 2^28 fits in int
@@ -271,6 +276,8 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
   __shared__ int s_wcnt[kScatterWarps][MOE_MAX_EXPERTS];
   __shared__ int s_pos[64 * MOE_MAX_TOPK];
 
+  griddep_wait();  // ids and the block histogram come from the previous kernel
+  griddep_launch_dependents();
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = T * k;
@@ -402,7 +409,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
 template <int NT, int KMAX>
 static cudaError_t launch_route_nt(const uint16_t* x, const uint4* wpack, const float* bias,
                                   const moe_dims& d, int32_t* ids, float* w, int32_t* hist,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, bool pdl) {
   const int TB = route_block_tokens(d.T);
   constexpr size_t smem = static_cast<size_t>(8) * NT * 4 * 32 * sizeof(float);
   if (smem > 48 * 1024) {
@@ -417,30 +424,29 @@ static cudaError_t launch_route_nt(const uint16_t* x, const uint4* wpack, const 
       attr_done[dev] = true;
     }
   }
-  route_kernel<NT, KMAX><<<route_blocks(d.T), kRouteThreads, smem, s>>>(x, wpack, bias, d.T, d.D, d.E,
-                                                                        d.k, TB, ids, w, hist);
-  note_launch();
-  return cudaGetLastError();
+  return launch_kernel(route_kernel<NT, KMAX>, dim3(route_blocks(d.T)), dim3(kRouteThreads), smem, s, pdl, x,
+                       wpack, bias, d.T, d.D, d.E, d.k, TB, ids, w, hist);
 }
 
 template <int NT>
 static cudaError_t launch_route_k(const uint16_t* x, const uint4* wpack, const float* bias,
                                  const moe_dims& d, int32_t* ids, float* w, int32_t* hist,
                                  cudaStream_t s) {
-  if (d.k <= 2) return launch_route_nt<NT, 2>(x, wpack, bias, d, ids, w, hist, s);
-  if (d.k <= 4) return launch_route_nt<NT, 4>(x, wpack, bias, d, ids, w, hist, s);
-  if (d.k <= 8) return launch_route_nt<NT, 8>(x, wpack, bias, d, ids, w, hist, s);
-  return launch_route_nt<NT, 16>(x, wpack, bias, d, ids, w, hist, s);
+  // the router follows the weight-packing kernel of the same call
+  if (d.k <= 2) return launch_route_nt<NT, 2>(x, wpack, bias, d, ids, w, hist, s, true);
+  if (d.k <= 4) return launch_route_nt<NT, 4>(x, wpack, bias, d, ids, w, hist, s, true);
+  if (d.k <= 8) return launch_route_nt<NT, 8>(x, wpack, bias, d, ids, w, hist, s, true);
+  return launch_route_nt<NT, 16>(x, wpack, bias, d, ids, w, hist, s, true);
 }
 
 cudaError_t launch_route(const uint16_t* x, const uint16_t* Wg, const float* bias, const moe_dims& d,
-                         void* wpack_buf, int32_t* ids, float* w, int32_t* hist, cudaStream_t s) {
+                         void* wpack_buf, int32_t* ids, float* w, int32_t* hist, cudaStream_t s,
+                         bool pdl) {
   const int NT = route_expert_tiles(d.E);
   uint4* wpack = static_cast<uint4*>(wpack_buf);
   const int nslots = (d.D / 32) * NT * 32;
-  pack_router_weights_kernel<<<(nslots + 255) / 256, 256, 0, s>>>(Wg, d.D, d.E, NT, wpack);
-  note_launch();
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_kernel(pack_router_weights_kernel, dim3((nslots + 255) / 256), dim3(256), 0, s, pdl,
+                                Wg, d.D, d.E, NT, wpack);
   if (e != cudaSuccess) return e;
   switch (NT) {
     case 1: return launch_route_k<1>(x, wpack, bias, d, ids, w, hist, s);
@@ -451,22 +457,18 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* Wg, const float* bia
   }
 }
 
-cudaError_t launch_hist(const int32_t* ids, const moe_dims& d, int32_t* hist, cudaStream_t s) {
-  hist_kernel<<<route_blocks(d.T), 256, 0, s>>>(ids, d.T, d.k, d.E, route_block_tokens(d.T), hist);
-  note_launch();
-  return cudaGetLastError();
+cudaError_t launch_hist(const int32_t* ids, const moe_dims& d, int32_t* hist, cudaStream_t s, bool pdl) {
+  return launch_kernel(hist_kernel, dim3(route_blocks(d.T)), dim3(256), 0, s, pdl, ids, d.T, d.k, d.E,
+                       route_block_tokens(d.T), hist);
 }
 
 cudaError_t launch_scatter(const int32_t* ids, const int32_t* hist, const moe_dims& d, int32_t* counts,
                            int32_t* offsets, int32_t* perm, int32_t* inv, const uint16_t* x,
-                           uint16_t* x_sorted, cudaStream_t s) {
+                           uint16_t* x_sorted, cudaStream_t s, bool pdl) {
   const int nblk = route_blocks(d.T);
-  scatter_kernel<<<nblk, kScatterThreads, 0, s>>>(ids, hist, d.T, d.k, d.E, route_block_tokens(d.T), nblk,
-                                                  counts, offsets, perm, inv,
-                                                  reinterpret_cast<const uint4*>(x),
-                                                  reinterpret_cast<uint4*>(x_sorted), d.D);
-  note_launch();
-  return cudaGetLastError();
+  return launch_kernel(scatter_kernel, dim3(nblk), dim3(kScatterThreads), 0, s, pdl, ids, hist, d.T, d.k, d.E,
+                       route_block_tokens(d.T), nblk, counts, offsets, perm, inv,
+                       reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(x_sorted), d.D);
 }
 
 }  // namespace moe
