@@ -233,6 +233,65 @@ def run_reference(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args):
+    """Roofline placement of the two grouped GEMMs as F/D and the tokens per
+    expert vary (the sweeps the Chinchilla/MoE page recommends for placing
+    the MoE FFN on the roofline).  One JSON line per shape."""
+    import torch
+    from grouped_gemm_router_gb300 import build
+    build.build()
+    from grouped_gemm_router_gb300 import moe
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pk, pk_kind = peaks()
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    E, k = 8, 2
+    shapes = []
+    if args.sweep in ("fd", "all"):   # F/D at a fixed 8192 tokens per expert
+        shapes += [("fd", 32768, 768, F) for F in (384, 768, 1536, 3072, 6144)]
+    if args.sweep in ("t", "all"):    # tokens per expert t = T*k/E at D=768, F=1536
+        shapes += [("t", T, 768, 1536) for T in (256, 1024, 4096, 16384, 65536)]
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for kind, T, D, F in shapes:
+        w, L = inputs.make_custom(T, D, F, E, k, False, 7)
+        G = {key: to_dev(v, dev) for key, v in L.items()}
+        ws = moe.Workspace(T, D, F, E, k, False, device=dev)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+        for row in evs:
+            for ev in row:
+                ev.record()
+        for _ in range(args.warmup):
+            moe.moe_ffn_forward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], k, workspace=ws)
+        for i in range(args.steps):
+            flush.fill_(1.0)
+            moe.moe_ffn_forward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], k, workspace=ws,
+                                stage_events=evs[i])
+        torch.cuda.synchronize()
+        t13 = float(np.mean([evs[i][2].elapsed_time(evs[i][3]) for i in range(args.steps)])) / 1e3
+        t2 = float(np.mean([evs[i][3].elapsed_time(evs[i][4]) for i in range(args.steps)])) / 1e3
+        S = T * k
+        t = S / E
+        # algorithmic work: each tensor read or written once
+        fl13, fl2 = 4 * S * D * F, 2 * S * F * D
+        by13 = S * D * 2 + 2 * E * D * F * 2 + S * F * 2
+        by2 = S * F * 2 + E * F * D * 2 + S * D * 2
+        line = {"sweep": kind, "T": T, "D": D, "F": F, "E": E, "k": k, "tokens_per_expert": t,
+                "F_over_D": F / D,
+                "w1w3": {"us": t13 * 1e6, "tflops": fl13 / t13 / 1e12, "gbs": by13 / t13 / 1e9,
+                         "intensity": fl13 / by13, "frac_tensor": fl13 / t13 / 1e12 / pk["bf16_tflops"],
+                         "frac_hbm": by13 / t13 / 1e9 / pk["hbm_gbs"]},
+                "w2": {"us": t2 * 1e6, "tflops": fl2 / t2 / 1e12, "gbs": by2 / t2 / 1e9,
+                       "intensity": fl2 / by2, "frac_tensor": fl2 / t2 / 1e12 / pk["bf16_tflops"],
+                       "frac_hbm": by2 / t2 / 1e9 / pk["hbm_gbs"]},
+                # the page's per-expert traffic model of the unfused up / down pair
+                "page_unfused_bytes_per_expert": 4 * t * D + 4 * t * F + 4 * D * F,
+                "page_fused_bytes_per_expert": 4 * t * D + 4 * D * F,
+                "ridge_flop_per_byte": ridge, "peaks": pk_kind}
+        print(json.dumps(line), flush=True)
+        del G, ws
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -241,7 +300,12 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=list(inputs.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", choices=["fd", "t", "all"], default=None,
+                    help="roofline placement of the grouped GEMMs over F/D or tokens per expert")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
 
