@@ -49,6 +49,8 @@
 //     16-deep slice starts 2048 k bytes into the tile.
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include "moe_device.cuh"
 #include "moe_kernels.cuh"
 
@@ -428,7 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-cudaError_t get_encoder() {
+// Guards the lazily filled per-process / per-device state below.
+std::mutex g_setup_mu;
+
+cudaError_t get_encoder() {  // caller holds g_setup_mu
   if (g_encode != nullptr) return cudaSuccess;
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
@@ -485,11 +490,15 @@ cudaError_t launch_pair(int nclusters, const CUtensorMap& a, const CUtensorMap& 
   return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kSwiGLU>, a, as, b0, b1, b0s, b1s, c, args);
 }
 
-cudaError_t device_setup(int* sms) {
+// One-time set-up of the current device (kernel attributes, co-resident
+// cluster counts, the tensor-map encoder); returns a copy of its state.
+cudaError_t device_setup(DeviceInfo* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  if ((e = get_encoder()) != cudaSuccess) return e;
   DeviceInfo& di = g_dev[dev];
   if (!di.attrs_set) {
     e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
@@ -518,14 +527,8 @@ cudaError_t device_setup(int* sms) {
     }
     di.attrs_set = true;
   }
-  *sms = di.sms;
+  *out = di;
   return cudaSuccess;
-}
-
-int pair_clusters(bool swiglu) {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  return g_dev[dev].pair_clusters[swiglu ? 1 : 0];
 }
 
 }  // namespace
@@ -534,10 +537,9 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
                                   const uint16_t* W3, const uint16_t* Ws1, const uint16_t* Ws3,
                                   const int32_t* offsets, const moe_dims& d, uint16_t* h,
                                   cudaStream_t s, bool pdl) {
-  cudaError_t e = get_encoder();
+  DeviceInfo di;
+  cudaError_t e = device_setup(&di);
   if (e != cudaSuccess) return e;
-  int sms = 0;
-  if ((e = device_setup(&sms)) != cudaSuccess) return e;
   const int S = d.T * d.k;
   const bool shared = Ws1 != nullptr;
   const int hw = 128;  // the last tile is half empty when F % 128 == 64
@@ -568,7 +570,7 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
   if ((e = make_map(&mC, h, static_cast<uint64_t>(S) + (shared ? d.T : 0), d.F, kOutBoxRows, kOutBoxCols)) !=
       cudaSuccess)
     return e;
-  e = launch_pair<true>(pair_clusters(true), mA, mAs, mB0, mB1, mB0s, mB1s, mC, a, s, pdl);
+  e = launch_pair<true>(di.pair_clusters[1], mA, mAs, mB0, mB1, mB0s, mB1s, mC, a, s, pdl);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -576,10 +578,9 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
 cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uint16_t* Ws2,
                                 const int32_t* offsets, const moe_dims& d, uint16_t* y,
                                 cudaStream_t s, bool pdl) {
-  cudaError_t e = get_encoder();
+  DeviceInfo di;
+  cudaError_t e = device_setup(&di);
   if (e != cudaSuccess) return e;
-  int sms = 0;
-  if ((e = device_setup(&sms)) != cudaSuccess) return e;
   const int S = d.T * d.k;
   const bool shared = Ws2 != nullptr;
   // D % 128 == 64: 128-wide tiles, the last one half empty
@@ -605,7 +606,7 @@ cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uin
   a.C = y;
   CUtensorMap mC;
   if ((e = make_map(&mC, y, hrows, d.D, kOutBoxRows, kOutBoxCols)) != cudaSuccess) return e;
-  e = launch_pair<false>(pair_clusters(false), mA, mA, mB0, mB0, mB0s, mB0s, mC, a, s, pdl);
+  e = launch_pair<false>(di.pair_clusters[0], mA, mA, mB0, mB0, mB0s, mB0s, mC, a, s, pdl);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }

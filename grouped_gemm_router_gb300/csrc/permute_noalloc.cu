@@ -21,6 +21,8 @@
 //  * The first call on each device resolves the array's device address with
 //    cudaGetSymbolAddress while that device is current.  Make that first call
 //    before any stream capture.
+#include <mutex>
+
 #include "moe_kernels.cuh"
 
 namespace moe {
@@ -37,11 +39,14 @@ int32_t* g_hist_ptr[kMaxDevices] = {nullptr};
 
 // Device address of the scratch array on the current device (set-up on the
 // first call per device).
+std::mutex g_scratch_mu;
+
 cudaError_t scratch_address(int32_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (g_hist_ptr[dev] == nullptr) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_hist);

@@ -11,6 +11,8 @@
 // far too narrow for a tcgen05 tile and the kernel is bound by reading x.
 #include <math.h>
 
+#include <mutex>
+
 #include "moe_device.cuh"
 #include "moe_kernels.cuh"
 
@@ -414,9 +416,11 @@ static cudaError_t launch_route_nt(const uint16_t* x, const uint4* wpack, const 
   constexpr size_t smem = static_cast<size_t>(8) * NT * 4 * 32 * sizeof(float);
   if (smem > 48 * 1024) {
     static bool attr_done[64] = {false};
+    static std::mutex mu;
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
     if (!attr_done[dev]) {
       cudaError_t e = cudaFuncSetAttribute(route_kernel<NT, KMAX>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -139,3 +139,38 @@ def test_forward_zero_tokens_is_a_no_op(moe):
     x0 = G["x"][:0]
     out = moe.moe_ffn_forward(x0, G["Wg"], G["W1"], G["W3"], G["W2"], 1)
     assert out.shape == (0, 64)
+
+
+def test_concurrent_calls_from_host_threads(moe):
+    """The library is re-entrant: host threads calling the layer at once on
+    their own streams and workspaces get the single-threaded result."""
+    import threading
+    w_, L = inputs.make_custom(2000, 256, 512, 8, 2, True, 55)
+    G = _dev_layer(L)
+    T, D, F, E, k = w_.T, w_.D, w_.F, w_.E, w_.k
+    ref = moe.moe_ffn_forward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], k, Ws1=G["Ws1"], Ws3=G["Ws3"],
+                              Ws2=G["Ws2"])
+    torch.cuda.synchronize()
+    outs, errors = [None] * 4, []
+
+    def worker(i):
+        try:
+            s = torch.cuda.Stream()
+            ws = moe.Workspace(T, D, F, E, k, True)
+            with torch.cuda.stream(s):
+                for _ in range(3):
+                    outs[i] = moe.moe_ffn_forward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], k, Ws1=G["Ws1"],
+                                                  Ws3=G["Ws3"], Ws2=G["Ws2"], workspace=ws)
+            s.synchronize()
+        except Exception as exc:  # pragma: no cover
+            errors.append(exc)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors
+    for o in outs:
+        assert torch.equal(o, ref)
+    assert moe.device_error() == 0
