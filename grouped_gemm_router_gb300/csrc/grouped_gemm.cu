@@ -97,7 +97,7 @@ constexpr int kPairStageBytes = kPairABytes + kPairBBytesMax;
 constexpr int kOutBoxRows = 32;                 // one epilogue warp's rows
 constexpr int kOutBoxCols = 32;                 // columns per TMA store box (64 bytes)
 constexpr int kOutBoxBytes = kOutBoxRows * kOutBoxCols * 2;
-constexpr int kOutBufs = kEpiWarps <= 8 ? 2 : 1; // staging buffers per epilogue warp
+constexpr int kOutBufs = 1;                      // staging buffers per epilogue warp
 constexpr int kPairSmemBytes =
     kPairStages * kPairStageBytes + kEpiWarps * kOutBufs * kOutBoxBytes + 1024;
 
