@@ -20,6 +20,9 @@ MOE_ERR_CUDA = -3
 MOE_ERR_WORKSPACE = -4
 MOE_ERR_DEVICE_TIMEOUT = -5
 
+MOE_FFN_CHAINED = 1
+CHAINED_MAX_D = 256
+
 MAX_EXPERTS = 128
 MAX_TOPK = 16
 MAX_DIM = 8192
@@ -33,7 +36,8 @@ class MoeDims(ctypes.Structure):
 class MoeOptions(ctypes.Structure):
     _fields_ = [("stage_events", ctypes.c_void_p * 8),
                 ("ids_in", ctypes.c_void_p),
-                ("weights_in", ctypes.c_void_p)]
+                ("weights_in", ctypes.c_void_p),
+                ("flags", ctypes.c_uint32)]
 
 
 class MoeError(RuntimeError):
@@ -57,6 +61,7 @@ _SIGNATURES = {
     "moe_permute": (_i32, [_vp, MoeDims, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_grouped_swiglu": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, MoeDims, _vp, _vp]),
     "moe_grouped_down": (_i32, [_vp, _vp, _vp, _vp, MoeDims, _vp, _vp]),
+    "moe_grouped_ffn_chained": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, MoeDims, _vp, _vp]),
     "moe_combine": (_i32, [_vp, _vp, _vp, MoeDims, _i32, _vp, _vp]),
     "moe_permute_noalloc": (_i32, [_vp, MoeDims, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_device_error": (_i32, []),

@@ -533,6 +533,23 @@ cudaError_t device_setup(DeviceInfo* out) {
 
 }  // namespace
 
+cudaError_t tensor_map_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                          uint32_t box_rows, uint32_t box_cols) {
+  {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
+  }
+  return make_map(m, ptr, rows, cols, box_rows, box_cols);
+}
+
+cudaError_t device_error_address(unsigned int** p) {
+  void* a = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&a, g_device_error);
+  *p = static_cast<unsigned int*>(a);
+  return e;
+}
+
 cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, const uint16_t* W1,
                                   const uint16_t* W3, const uint16_t* Ws1, const uint16_t* Ws3,
                                   const int32_t* offsets, const moe_dims& d, uint16_t* h,

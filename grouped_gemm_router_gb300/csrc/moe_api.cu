@@ -110,11 +110,17 @@ moe_status run_layer(const uint16_t* x, const uint16_t* Wg, const float* bias, c
   e = launch_scatter(ids, ws.hist, d, ws.counts, ws.offsets, ws.perm, ws.inv, x, ws.x_sorted, s, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(o, 2, s);
-  e = launch_grouped_swiglu(ws.x_sorted, x, W1, W3, Ws1, Ws3, ws.offsets, d, ws.h, s, true);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  record(o, 3, s);
-  e = launch_grouped_down(ws.h, W2, Ws2, ws.offsets, d, ws.y, s, true);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (o != nullptr && (o->flags & MOE_FFN_CHAINED)) {
+    e = launch_chained_ffn(ws.x_sorted, x, W1, W3, W2, Ws1, Ws3, Ws2, ws.offsets, d, ws.y, s, true);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    record(o, 3, s);
+  } else {
+    e = launch_grouped_swiglu(ws.x_sorted, x, W1, W3, Ws1, Ws3, ws.offsets, d, ws.h, s, true);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    record(o, 3, s);
+    e = launch_grouped_down(ws.h, W2, Ws2, ws.offsets, d, ws.y, s, true);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
   record(o, 4, s);
   e = launch_combine(ws.y, w, ws.inv, d, shared ? 1 : 0, out, s, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -137,6 +143,9 @@ moe_status validate_layer(const void* x, const void* Wg, const float* bias, cons
   if (o != nullptr && ((o->ids_in == nullptr) != (o->weights_in == nullptr))) return MOE_ERR_INVALID_ARG;
   if (o != nullptr && o->ids_in != nullptr && (!aligned16(o->ids_in) || !aligned16(o->weights_in)))
     return MOE_ERR_INVALID_ARG;
+  if (o != nullptr && (o->flags & ~MOE_FFN_CHAINED) != 0) return MOE_ERR_INVALID_ARG;
+  if (o != nullptr && (o->flags & MOE_FFN_CHAINED) && d.D > MOE_CHAINED_MAX_D)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
   return MOE_OK;
 }
 
@@ -266,6 +275,28 @@ moe_status moe_grouped_swiglu(const void* x_sorted, const void* x, const void* W
       static_cast<const uint16_t*>(W1), static_cast<const uint16_t*>(W3),
       static_cast<const uint16_t*>(Ws1), static_cast<const uint16_t*>(Ws3), offsets, d,
       static_cast<uint16_t*>(h), static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_grouped_ffn_chained(const void* x_sorted, const void* x, const void* W1,
+                                   const void* W3, const void* W2, const void* Ws1,
+                                   const void* Ws3, const void* Ws2, const int32_t* offsets,
+                                   moe_dims d, void* y, void* stream) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d.D > MOE_CHAINED_MAX_D) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!x_sorted || !W1 || !W3 || !W2 || !offsets || !y) return MOE_ERR_INVALID_ARG;
+  if (shared_state(Ws1, Ws3, Ws2) < 0) return MOE_ERR_INVALID_ARG;
+  if (Ws1 != nullptr && x == nullptr) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x_sorted, x, W1, W3, W2, Ws1, Ws3, Ws2, y};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (d.T == 0) return MOE_OK;
+  return cuda_status(launch_chained_ffn(
+      static_cast<const uint16_t*>(x_sorted), static_cast<const uint16_t*>(x),
+      static_cast<const uint16_t*>(W1), static_cast<const uint16_t*>(W3),
+      static_cast<const uint16_t*>(W2), static_cast<const uint16_t*>(Ws1),
+      static_cast<const uint16_t*>(Ws3), static_cast<const uint16_t*>(Ws2), offsets, d,
+      static_cast<uint16_t*>(y), static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_grouped_down(const void* h, const void* W2, const void* Ws2, const int32_t* offsets,

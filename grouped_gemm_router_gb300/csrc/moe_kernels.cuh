@@ -1,6 +1,7 @@
 // Host-side launchers shared between the translation units of the library.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -63,6 +64,26 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
 cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uint16_t* Ws2,
                                 const int32_t* offsets, const moe_dims& d, uint16_t* y,
                                 cudaStream_t s, bool pdl = false);
+
+// W1||W3 + SiLU*mul and W2 chained in one kernel (chained_ffn.cu): same
+// inputs as the two grouped GEMMs, y [S (+T), D] out, h never stored.
+// Requires D <= kChainedMaxD.
+constexpr int kChainedMaxD = 256;
+cudaError_t launch_chained_ffn(const uint16_t* x_sorted, const uint16_t* x, const uint16_t* W1,
+                               const uint16_t* W3, const uint16_t* W2, const uint16_t* Ws1,
+                               const uint16_t* Ws3, const uint16_t* Ws2, const int32_t* offsets,
+                               const moe_dims& d, uint16_t* y, cudaStream_t s, bool pdl = false);
+
+// 2-D bf16 TMA descriptor of a row-major [rows, cols] matrix with a
+// {box_cols, box_rows} box: 128-byte swizzle (64-byte for 32-column boxes),
+// zero fill outside the tensor (grouped_gemm.cu).
+cudaError_t tensor_map_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                          uint32_t box_rows, uint32_t box_cols);
+
+// Device address of the error word that moe_device_error reads, on the
+// current device.
+cudaError_t device_error_address(unsigned int** p);
+
 // One-CTA kernel whose bounded mbarrier wait must time out (*gave_up = 1).
 cudaError_t launch_wait_timeout_selftest(uint64_t timeout_ns, int* gave_up, cudaStream_t s);
 // Reads and clears the device error word (synchronous).

@@ -88,10 +88,11 @@ class Workspace:
         return out
 
 
-def _options(stage_events=None, ids_in=None, weights_in=None):
-    if stage_events is None and ids_in is None:
+def _options(stage_events=None, ids_in=None, weights_in=None, chained=False):
+    if stage_events is None and ids_in is None and not chained:
         return None
     o = N.MoeOptions()
+    o.flags = N.MOE_FFN_CHAINED if chained else 0
     for i, ev in enumerate(stage_events or []):
         if ev is None:
             continue
@@ -111,8 +112,10 @@ def _options(stage_events=None, ids_in=None, weights_in=None):
 
 def moe_ffn_forward(x, Wg, W1, W3, W2, k, bias=None, Ws1=None, Ws3=None, Ws2=None, out=None,
                     workspace: Workspace | None = None, stage_events=None, ids_in=None,
-                    weights_in=None):
-    """Forward pass of the MoE SwiGLU FFN layer; returns out [T, D] bf16."""
+                    weights_in=None, chained=False):
+    """Forward pass of the MoE SwiGLU FFN layer; returns out [T, D] bf16.
+    chained=True runs W1||W3 and W2 as one kernel with h kept on chip
+    (D <= 256)."""
     T, D, F, E, k = layer_dims(x, W1, k)
     shared = Ws1 is not None
     for t, n, shp in ((x, "x", (T, D)), (Wg, "Wg", (D, E)), (W1, "W1", (E, D, F)),
@@ -127,7 +130,7 @@ def moe_ffn_forward(x, Wg, W1, W3, W2, k, bias=None, Ws1=None, Ws3=None, Ws2=Non
     st = lib.moe_ffn_forward(_ptr(x), _ptr(Wg), _ptr(bias), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(Ws1),
                              _ptr(Ws3), _ptr(Ws2), N.dims(T, D, F, E, k), _ptr(out),
                              _ptr(workspace.buf), workspace.nbytes,
-                             _options(stage_events, ids_in, weights_in), _stream())
+                             _options(stage_events, ids_in, weights_in, chained), _stream())
     check(st, "moe_ffn_forward")
     return out
 
@@ -227,6 +230,33 @@ def moe_grouped_down(h, offsets, W2, T, k, Ws2=None, y=None):
     st = lib.moe_grouped_down(_ptr(h), _ptr(W2), _ptr(Ws2), _ptr(offsets), N.dims(T, D, F, E, k),
                               _ptr(y), _stream())
     check(st, "moe_grouped_down")
+    return y
+
+
+def moe_grouped_ffn_chained(x_sorted, offsets, W1, W3, W2, T, k, x=None, Ws1=None, Ws3=None,
+                            Ws2=None, y=None):
+    """y [T*k (+T), D] = (silu(A W1[e]) * (A W3[e])) W2[e] per expert group
+    (+ shared rows), in one kernel that never writes h (D <= 256)."""
+    S, D = x_sorted.shape
+    E, _, F = W1.shape
+    shared = Ws1 is not None
+    _need(x_sorted, "x_sorted", torch.bfloat16, (T * k, D))
+    _need(W1, "W1", torch.bfloat16, (E, D, F))
+    _need(W3, "W3", torch.bfloat16, (E, D, F))
+    _need(W2, "W2", torch.bfloat16, (E, F, D))
+    _need(offsets, "offsets", torch.int32, (E + 1,))
+    if shared:
+        _need(x, "x", torch.bfloat16, (T, D))
+        _need(Ws1, "Ws1", torch.bfloat16, (D, F))
+        _need(Ws3, "Ws3", torch.bfloat16, (D, F))
+        _need(Ws2, "Ws2", torch.bfloat16, (F, D))
+    rows = T * k + (T if shared else 0)
+    if y is None:
+        y = torch.empty(rows, D, dtype=torch.bfloat16, device=x_sorted.device)
+    st = lib.moe_grouped_ffn_chained(_ptr(x_sorted), _ptr(x), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(Ws1),
+                                     _ptr(Ws3), _ptr(Ws2), _ptr(offsets), N.dims(T, D, F, E, k), _ptr(y),
+                                     _stream())
+    check(st, "moe_grouped_ffn_chained")
     return y
 
 

@@ -80,7 +80,15 @@ typedef struct {
    * device memory replace the router when both are non-NULL. */
   const int32_t* ids_in;
   const float* weights_in;
+  /* MOE_FFN_CHAINED: run W1||W3 and W2 as one chained kernel that keeps h on
+   * chip (moe_grouped_ffn_chained); needs D <= MOE_CHAINED_MAX_D.  The h
+   * region of the workspace is then left untouched, and stage_events[3] is
+   * recorded together with [4] after the chained kernel. */
+  uint32_t flags;
 } moe_ffn_options;
+
+#define MOE_FFN_CHAINED 1u
+#define MOE_CHAINED_MAX_D 256
 
 /* Bytes of device workspace moe_ffn_forward needs for these dimensions
  * (has_shared != 0 when the shared expert is used; host_io != 0 adds the
@@ -167,6 +175,21 @@ moe_status moe_grouped_swiglu(const void* x_sorted, const void* x, const void* W
  * y[T*k + t] = h[T*k + t] Ws2.  y holds T*k (+T) rows of D bf16. */
 moe_status moe_grouped_down(const void* h, const void* W2, const void* Ws2, const int32_t* offsets,
                             moe_dims d, void* y, void* stream);
+
+/* W1||W3 + SiLU*mul and W2 chained in one kernel, h never written to memory
+ * ("Chinchilla scaling, MoE, and fused Triton kernels", sections "Fused Triton
+ * kernel mechanism" and "Triton fused kernel implementation").  Same inputs as
+ * moe_grouped_swiglu and moe_grouped_down together, same output y [T*k (+T), D]
+ * bf16: per 256-row tile the kernel streams F in 64-column chunks, rounds each
+ * h chunk to bf16 in shared memory and accumulates y in fp32 over the chunks
+ * in the order of the two separate GEMMs, so y equals their result.
+ * MOE_ERR_UNSUPPORTED_SHAPE when D > MOE_CHAINED_MAX_D: a tile's y
+ * accumulator (D fp32 columns per row) and two g|u buffers (128 columns each)
+ * must fit in the 512 TMEM columns of an SM. */
+moe_status moe_grouped_ffn_chained(const void* x_sorted, const void* x, const void* W1,
+                                   const void* W3, const void* W2, const void* Ws1,
+                                   const void* Ws3, const void* Ws2, const int32_t* offsets,
+                                   moe_dims d, void* y, void* stream);
 
 /* Weighted combine ("PyTorch MoE implementation": inverse permutation and
  * weighted sum): out[t] = sum_j weights[t, j] * y[inv[t*k + j]]

@@ -77,6 +77,22 @@ def test_argument_validation_before_launch(native):
                                     p(FAKE), None) == N.MOE_ERR_INVALID_ARG     # shared needs x
     assert N.lib.moe_combine(p(FAKE), p(FAKE), p(FAKE), N.dims(4, 96, 64, 4, 2), 0, p(FAKE),
                              None) == N.MOE_ERR_UNSUPPORTED_SHAPE
+    # the chained kernel keeps a D-column fp32 accumulator in TMEM: D <= 256
+    chained = lambda d, x=FAKE, shared=(None, None, None): N.lib.moe_grouped_ffn_chained(
+        p(FAKE), p(x) if x else None, p(FAKE), p(FAKE), p(FAKE), *(p(s) if s else None for s in shared),
+        p(FAKE), d, p(FAKE), None)
+    assert chained(N.dims(256, 320, 256, 4, 2)) == N.MOE_ERR_UNSUPPORTED_SHAPE
+    assert chained(good, x=0, shared=(FAKE, FAKE, FAKE)) == N.MOE_ERR_INVALID_ARG   # shared needs x
+    assert chained(good, shared=(FAKE, FAKE, None)) == N.MOE_ERR_INVALID_ARG        # partial shared
+    assert chained(N.dims(0, 128, 256, 4, 2)) == N.MOE_OK
+    opts = N.MoeOptions()
+    opts.flags = N.MOE_FFN_CHAINED
+    fwd = lambda d, o: N.lib.moe_ffn_forward(p(FAKE), p(FAKE), None, p(FAKE), p(FAKE), p(FAKE), None,
+                                             None, None, d, p(FAKE), p(FAKE), 1 << 40, ctypes.byref(o),
+                                             None)
+    assert fwd(N.dims(256, 512, 256, 4, 2), opts) == N.MOE_ERR_UNSUPPORTED_SHAPE
+    opts.flags = 2   # no such flag
+    assert fwd(good, opts) == N.MOE_ERR_INVALID_ARG
     assert N.lib.moe_selftest_wait_timeout(0, p(FAKE), None) == N.MOE_ERR_INVALID_ARG
     assert N.lib.moe_selftest_wait_timeout(10, None, None) == N.MOE_ERR_INVALID_ARG
     assert N.lib.moe_launch_count() == 0
