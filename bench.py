@@ -292,6 +292,71 @@ def run_sweep(args):
         del G, ws
 
 
+def run_chain_sweep(args):
+    """Chained (h kept on chip) vs unchained (h through HBM) expert FFN as F/D
+    and the tokens per expert vary: the sweeps the fused-Triton-kernel page
+    proposes to place the fused kernel on the roofline.  One JSON line per
+    shape; times are CUDA events around the expert stage(s) of the layer."""
+    import torch
+    from grouped_gemm_router_gb300 import build
+    build.build()
+    from grouped_gemm_router_gb300 import moe
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pk, pk_kind = peaks()
+    E, k = 8, 2
+    shapes = [("chain_fd", 2048, 256, F) for F in (256, 512, 1024, 2048, 4096)]
+    shapes += [("chain_fd", 32768, 256, F) for F in (256, 1024, 4096)]
+    shapes += [("chain_t", T, 256, 1024) for T in (256, 1024, 4096, 16384, 65536)]
+    shapes += [("chain_t", T, 128, 1024) for T in (1024, 16384)]
+    if args.chain_shape:  # one shape, e.g. for a DRAM-counter capture
+        T, D, F = (int(v) for v in args.chain_shape.split("x"))
+        shapes = [("chain_one", T, D, F)]
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+    for kind, T, D, F in shapes:
+        w, L = inputs.make_custom(T, D, F, E, k, False, 7)
+        G = {key: to_dev(v, dev) for key, v in L.items()}
+        ws = moe.Workspace(T, D, F, E, k, False, device=dev)
+        res = {}
+        for chained in (False, True):
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+            for row in evs:
+                for ev in row:
+                    ev.record()
+            for _ in range(args.warmup):
+                moe.moe_ffn_forward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], k, workspace=ws,
+                                    chained=chained)
+            for i in range(args.steps):
+                flush.fill_(1.0)
+                sink.copy_(flush.sum())
+                moe.moe_ffn_forward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], k, workspace=ws,
+                                    stage_events=evs[i], chained=chained)
+            torch.cuda.synchronize()
+            res[chained] = float(np.mean([evs[i][2].elapsed_time(evs[i][4]) for i in range(args.steps)])) / 1e3
+        assert moe.device_error() == 0
+        S = T * k
+        t = S / E
+        flops = 6 * S * D * F
+        fused_bytes = S * D * 2 + 3 * E * D * F * 2 + S * D * 2
+        unfused_bytes = fused_bytes + 2 * S * F * 2
+        line = {"sweep": kind, "T": T, "D": D, "F": F, "E": E, "k": k, "tokens_per_expert": t,
+                "F_over_D": F / D,
+                "unchained_us": res[False] * 1e6, "chained_us": res[True] * 1e6,
+                "speedup": res[False] / res[True],
+                "unchained_tflops": flops / res[False] / 1e12, "chained_tflops": flops / res[True] / 1e12,
+                "unchained_frac_tensor": flops / res[False] / 1e12 / pk["bf16_tflops"],
+                "chained_frac_tensor": flops / res[True] / 1e12 / pk["bf16_tflops"],
+                "intensity_unfused": flops / unfused_bytes, "intensity_fused": flops / fused_bytes,
+                "unfused_bytes": unfused_bytes, "fused_bytes": fused_bytes,
+                # the page's model of the speedup while memory-bound
+                "page_model_speedup": 1 + t * F / (t * D + D * F),
+                "ridge_flop_per_byte": pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9), "peaks": pk_kind}
+        print(json.dumps(line), flush=True)
+        del G, ws
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -300,9 +365,15 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=list(inputs.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--sweep", choices=["fd", "t", "all"], default=None,
-                    help="roofline placement of the grouped GEMMs over F/D or tokens per expert")
+    ap.add_argument("--sweep", choices=["fd", "t", "all", "chained"], default=None,
+                    help="roofline placement of the grouped GEMMs over F/D or tokens per expert; "
+                         "'chained': chained vs unchained expert FFN (D <= 256)")
+    ap.add_argument("--chain-shape", default=None, metavar="TxDxF",
+                    help="with --sweep chained: measure this one shape only")
     args = ap.parse_args()
+    if args.sweep == "chained":
+        run_chain_sweep(args)
+        return
     if args.sweep:
         run_sweep(args)
         return

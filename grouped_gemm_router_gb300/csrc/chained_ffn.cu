@@ -54,15 +54,16 @@ namespace {
 constexpr int kBK = 64;                          // k per staged block (128 bytes of bf16)
 constexpr int kFC = 64;                          // h columns per chunk
 constexpr int kMaxD = kChainedMaxD;
-constexpr int kStages = 6;
+constexpr int kStages = 7;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxGroups = MOE_MAX_EXPERTS + 1;
 constexpr int kTileRows = 256;                   // rows per pair tile
 constexpr int kABlock = 128 * kBK * 2;           // 16 KB: a 64-deep block of this CTA's rows
 constexpr int kABytes = kMaxD / kBK * kABlock;   // resident x rows
+constexpr int kBK1 = 128;                        // k per staged W1 / W3 block
 constexpr int kBoxBytes = 64 * 64 * 2;           // one 64 x 64 weight box
-constexpr int kStageBytes = 2 * kBoxBytes;       // W1 or W3 block: 1 box; W2 block: <= 2 boxes
+constexpr int kStageBytes = 2 * kBoxBytes;       // W1 or W3: 128 k x 64 n; W2: 64 k x <= 128 n
 constexpr int kHBytes = 128 * kFC * 2;           // 16 KB: one h chunk of this CTA's rows
 constexpr int kOutBoxRows = 32;
 constexpr int kOutBoxCols = 32;
@@ -75,7 +76,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemGU = 2 * kFC;            // columns of one g|u buffer
 constexpr uint32_t kTmemY = 2 * kTmemGU;         // Y at columns [256, 256 + D)
 static_assert(kTmemY + kMaxD <= kTmemCols, "TMEM budget");
-static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
 
 struct ChainArgs {
   const int32_t* offsets;  // [E + 1]
@@ -107,6 +107,8 @@ struct ChainCtl {
   int row0[kMaxGroups];
   int nrows[kMaxGroups];
 };
+// dynamic (with its 1 KB alignment slack) + static shared memory of one CTA
+static_assert(kSmemBytes + sizeof(ChainCtl) <= 227 * 1024, "shared-memory budget");
 
 __global__ void __launch_bounds__(kThreads, 1)
     chained_ffn_pair_kernel(const __grid_constant__ CUtensorMap mapA,
@@ -130,7 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pair = static_cast<int>(cluster_id_x());
   const int npairs = static_cast<int>(num_clusters_x());
   const int G = p.E + (p.T_shared > 0 ? 1 : 0);
-  const int nkb = p.D / kBK;       // 64-deep blocks of G1
+  const int nkb = p.D / kBK;       // 64-deep blocks of the resident x rows
+  const int nst1 = (p.D + kBK1 - 1) / kBK1;  // W1 / W3 stages per chunk
   const int nch = p.F / kFC;       // F chunks
   const int halfD = p.D / 2;       // Y columns of W2 staged by this CTA
   const int nbox2 = (halfD + 63) / 64;
@@ -218,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_a = l2_policy_evict_normal();
       const uint64_t pol_b = l2_policy_evict_last();
       const uint32_t a_tx = 2u * static_cast<uint32_t>(nkb * kABlock);
-      const uint32_t b1_tx = 2u * kBoxBytes;
+      const uint32_t b1_tx = 2u * kStageBytes;
       const uint32_t b2_tx = 2u * static_cast<uint32_t>(nbox2 * kBoxBytes);
       int stage = 0;
       uint32_t phase = 0;
@@ -247,15 +250,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* mB2 = routed ? &mapW2 : &mapW2s;
         for (int c = 0; c <= nch && ok; ++c) {
           if (c < nch) {  // W1 (leader) / W3 (peer) blocks of chunk c
-            for (int kb = 0; kb < nkb; ++kb) {
+            for (int s1 = 0; s1 < nst1; ++s1) {
               if (!mbar_wait_cluster(smem_u32(&ctl.empty[stage]), phase ^ 1u, abort_flag, dev_err)) {
                 ok = false;
                 break;
               }
               const uint32_t full_leader = map_to_cta(smem_u32(&ctl.full[stage]), 0);
               if (leader) mbar_arrive_expect_tx(smem_u32(&ctl.full[stage]), b1_tx);
+              // 128 k-rows (the last block of an odd number of 64-row blocks
+              // also reads 64 rows past it, which no MMA uses)
               tma_load_2d_pair(sbase + kOffStages + stage * kStageBytes, mB1, full_leader, c * kFC,
-                               w1_row + kb * kBK, pol_b);
+                               w1_row + s1 * kBK1, pol_b);
               ++issued;
               if (++stage == kStages) {
                 stage = 0;
@@ -323,19 +328,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after_sync();
             const uint32_t d_tmem = tmem_base + b * kTmemGU;
-            for (int kb = 0; kb < nkb; ++kb) {
+            for (int s1 = 0; s1 < nst1; ++s1) {
               if (!mbar_wait_cluster(smem_u32(&ctl.full[stage]), phase, abort_flag, dev_err)) {
                 ok = false;
                 break;
               }
               tc_fence_after_sync();
-              const uint32_t sa = sbase + kb * kABlock;
               const uint32_t sb = sbase + kOffStages + stage * kStageBytes;
-#pragma unroll
-              for (int kk = 0; kk < kBK / 16; ++kk) {
-                const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
+              const int nk16 = min(kBK1, p.D - s1 * kBK1) / 16;
+              for (int kk = 0; kk < nk16; ++kk) {
+                // k = 128 s1 + 16 kk: resident x block 2 s1 + kk / 4, slice kk % 4
+                const uint32_t sa = sbase + (2 * s1 + (kk >> 2)) * kABlock + (kk & 3) * 32;
+                const uint64_t adesc = smem_desc_sw128(sa, 16, 1024);
                 const uint64_t bdesc = smem_desc_sw128(sb + kk * 2048, 8192, 1024);
-                umma_bf16_pair(d_tmem, adesc, bdesc, idesc1, (kb | kk) != 0 ? 1u : 0u);
+                umma_bf16_pair(d_tmem, adesc, bdesc, idesc1, (s1 | kk) != 0 ? 1u : 0u);
               }
               umma_commit_pair(smem_u32(&ctl.empty[stage]), 0x3);
               if (++stage == kStages) {
@@ -569,13 +575,13 @@ cudaError_t launch_chained_ffn(const uint16_t* x_sorted, const uint16_t* x, cons
   const uint64_t yrows = static_cast<uint64_t>(S) + (shared ? d.T : 0);
   CUtensorMap mA, mAs, mW1, mW3, mW1s, mW3s, mW2, mW2s, mY;
   if ((e = tensor_map_2d(&mA, x_sorted, S, d.D, 128, kBK)) != cudaSuccess) return e;
-  if ((e = tensor_map_2d(&mW1, W1, static_cast<uint64_t>(d.E) * d.D, d.F, kBK, 64)) != cudaSuccess) return e;
-  if ((e = tensor_map_2d(&mW3, W3, static_cast<uint64_t>(d.E) * d.D, d.F, kBK, 64)) != cudaSuccess) return e;
+  if ((e = tensor_map_2d(&mW1, W1, static_cast<uint64_t>(d.E) * d.D, d.F, kBK1, 64)) != cudaSuccess) return e;
+  if ((e = tensor_map_2d(&mW3, W3, static_cast<uint64_t>(d.E) * d.D, d.F, kBK1, 64)) != cudaSuccess) return e;
   if ((e = tensor_map_2d(&mW2, W2, static_cast<uint64_t>(d.E) * d.F, d.D, kFC, 64)) != cudaSuccess) return e;
   if (shared) {
     if ((e = tensor_map_2d(&mAs, x, d.T, d.D, 128, kBK)) != cudaSuccess) return e;
-    if ((e = tensor_map_2d(&mW1s, Ws1, d.D, d.F, kBK, 64)) != cudaSuccess) return e;
-    if ((e = tensor_map_2d(&mW3s, Ws3, d.D, d.F, kBK, 64)) != cudaSuccess) return e;
+    if ((e = tensor_map_2d(&mW1s, Ws1, d.D, d.F, kBK1, 64)) != cudaSuccess) return e;
+    if ((e = tensor_map_2d(&mW3s, Ws3, d.D, d.F, kBK1, 64)) != cudaSuccess) return e;
     if ((e = tensor_map_2d(&mW2s, Ws2, d.F, d.D, kFC, 64)) != cudaSuccess) return e;
   } else {
     mAs = mA;
