@@ -54,6 +54,9 @@ _SIGNATURES = {
                                ctypes.POINTER(MoeOptions), _vp]),
     "moe_ffn_forward_host": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, MoeDims, _vp, _vp,
                                     _sz, ctypes.POINTER(MoeOptions), _vp]),
+    "moe_ffn_backward_workspace_size": (_sz, [MoeDims, _i32]),
+    "moe_ffn_backward": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, MoeDims, _vp, _sz, _vp, _vp, _vp,
+                                _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, ctypes.POINTER(MoeOptions), _vp]),
     "moe_route_scratch_size": (_sz, [MoeDims]),
     "moe_route": (_i32, [_vp, _vp, _vp, MoeDims, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_route_block_tokens": (_i32, [_i32]),

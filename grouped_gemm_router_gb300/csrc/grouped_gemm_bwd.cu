@@ -1,0 +1,729 @@
+// Backward grouped GEMMs of the MoE SwiGLU FFN on tcgen05 CTA pairs.
+//
+// The backward of an expert y = (silu(x W1) * (x W3)) W2 over its rows
+// ("Triton MoE Kernels & Memory Checkpointing", Part A, section 8, the
+// autograd contract and its "dual kernels"): with y_bar the gradient of y,
+//   h_bar = y_bar W2^T                                        (W2 dgrad)
+//   g_bar = h_bar * u * silu'(g),  u_bar = h_bar * silu(g)    (activation)
+//   x_bar = g_bar W1^T + u_bar W3^T                           (x dgrad)
+//   W1_bar = x^T g_bar,  W3_bar = x^T u_bar,  W2_bar = h^T y_bar  (wgrad)
+// One persistent CTA-pair kernel (same engine as the forward grouped GEMM:
+// 256 x N pair tiles, 6 TMA stages, two TMEM accumulators, bounded waits)
+// runs four modes:
+//   kDgradW2  A = y_bar rows (K-major), B = W2[e]^T read K-major from the
+//             rows of W2 [E*F, D]; bf16 h_bar out.
+//   kActBwd   the W1||W3 forward recomputed (A = x_sorted, B = W1 | W3 as in
+//             the forward); the epilogue reads h_bar and writes g_bar | u_bar
+//             ([rows, 2F]) and the recomputed h ([rows, F]) in bf16.
+//   kDgradX   A = g_bar | u_bar rows (K = 2F, K-major), B = W1[e]^T for the
+//             first F and W3[e]^T for the rest, read K-major from the rows of
+//             W1 / W3 [E*D, F]; bf16 x_bar out.
+//   kWgrad    C[e] = A^T B over the rows of group e: A and B both M/N-major
+//             (row-major [rows, M] and [rows, N] tiles), K = the group's
+//             rows; fp32 out, zeros for an empty group.
+//
+// Row layouts.  The gradient buffers use a padded sorted layout: group e owns
+// rows [prow0_e, prow0_e + pn_e), pn_e = n_e rounded up to 64, prow0 the
+// exclusive prefix sum of pn; rows [n_e, pn_e) of y_bar are zero (the combine
+// backward writes them), so every derived gradient is zero there too and a
+// weight-gradient k-block never has to be masked.  x_sorted keeps the
+// forward's unpadded layout (rows offsets[e] ..).  The shared expert is one
+// more group whose operands have their own tensor maps over exactly T rows
+// (zero fill past T) and whose outputs go to rows S_pad .. S_pad + T.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "moe_device.cuh"
+#include "moe_kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kBK = 64;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kMaxGroups = MOE_MAX_EXPERTS + 1;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kTileM = 256;                   // rows per pair tile
+constexpr int kTileN = 256;                   // MMA N
+constexpr int kStages = 6;
+constexpr int kABytes = 128 * kBK * 2;        // 16 KB: this CTA's half of A per k-block
+constexpr int kBBytes = 128 * kBK * 2;        // 16 KB: this CTA's half of B per k-block
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kOutBoxRows = 32;
+constexpr int kOutBoxCols = 32;
+constexpr int kOutBoxBytes = kOutBoxRows * kOutBoxCols * 2;
+constexpr int kSmemBytes = kStages * kStageBytes + kEpiWarps * kOutBoxBytes + 1024;
+
+enum : int { kDgradW2 = 0, kActBwd = 1, kDgradX = 2, kWgrad = 3 };
+
+template <int kMode>
+struct Traits {
+  static constexpr bool a_mn = kMode == kWgrad;                       // A M-major
+  static constexpr bool b_mn = kMode == kActBwd || kMode == kWgrad;   // B N-major
+  static constexpr bool row_tiles = kMode != kWgrad;                  // tiles over rows
+};
+
+struct BwdArgs {
+  const int32_t* offsets;  // [E + 1] forward sorted-row offsets
+  int E;
+  int S;                   // routed rows T*k
+  int S_pad;               // first row of the shared group in the padded buffers
+  int T_shared;            // rows of the shared group (0: none)
+  int K;                   // row modes: reduction length (kDgradX: 2F)
+  int K1;                  // kDgradX: k at which B switches from W1 to W3 (= F)
+  int N;                   // output columns
+  int M;                   // kWgrad: output rows
+  int b_rows;              // K-major B: rows of one expert's weight block (row modes)
+  int a_padded;            // kWgrad: A rows in the padded layout (else unpadded)
+  uint16_t* C;             // kDgradW2 / kDgradX: bf16 output [S_pad + T, N] (mapC's tensor)
+  // kActBwd
+  const uint16_t* hbar;    // [S_pad + T, N] incoming gradient of h
+  uint16_t* gu;            // [S_pad + T, 2N] g_bar | u_bar
+  uint16_t* h;             // [S_pad + T, N] recomputed h
+  // kWgrad: fp32 outputs; columns [0, n_split) go to *_a, [n_split, N) to *_b
+  float* w_a;
+  float* w_b;
+  float* ws_a;
+  float* ws_b;
+  int n_split;
+  unsigned int* dev_err;
+};
+
+struct BwdCtl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int total_tiles;
+  int tile_prefix[kMaxGroups + 1];
+  int row0[kMaxGroups];   // unpadded first row (forward layout)
+  int prow0[kMaxGroups];  // padded first row (shared group: S_pad)
+  int nrows[kMaxGroups];
+  int pnrows[kMaxGroups];
+};
+
+// Reads one bf16 x 32 chunk (64 bytes) into 16 packed words.
+MOE_DEV void load_bf16x32(const uint16_t* src, uint32_t (&v)[16]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 q = s[i];
+    v[4 * i] = q.x;
+    v[4 * i + 1] = q.y;
+    v[4 * i + 2] = q.z;
+    v[4 * i + 3] = q.w;
+  }
+}
+
+MOE_DEV void store_bf16x32(uint16_t* dst, const uint32_t (&v)[16]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap mapA,
+                            const __grid_constant__ CUtensorMap mapA_sh,
+                            const __grid_constant__ CUtensorMap mapB0,
+                            const __grid_constant__ CUtensorMap mapB1,
+                            const __grid_constant__ CUtensorMap mapB0_sh,
+                            const __grid_constant__ CUtensorMap mapB1_sh,
+                            const __grid_constant__ CUtensorMap mapC, const BwdArgs p) {
+  using Tr = Traits<kMode>;
+  extern __shared__ uint8_t bwd_smem_raw[];
+  __shared__ BwdCtl ctl;
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(bwd_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t smem_base = smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(cluster_id_x());
+  const int npairs = static_cast<int>(num_clusters_x());
+  const int G = p.E + (p.T_shared > 0 ? 1 : 0);
+  // output columns per tile: kActBwd computes g and u of kTileN / 2 columns
+  const int hw = kMode == kActBwd ? kTileN / 2 : kTileN;
+  const int ntn = (p.N + hw - 1) / hw;
+  const int nmt = (p.M + kTileM - 1) / kTileM;  // kWgrad
+  const int half_n = kTileN / 2;
+
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapB0);
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(smem_u32(&ctl.full[st]), 1);
+      mbar_init(smem_u32(&ctl.empty[st]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ctl.tfull[b]), 1);
+      mbar_init(smem_u32(&ctl.tempty[b]), 2 * kEpiWarps);
+    }
+    mbar_init(smem_u32(&ctl.drain), 1);
+    ctl.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&ctl.tmem_base), kTmemCols);
+    tmem_relinquish_pair();
+    tc_fence_before_sync();
+  }
+  griddep_launch_dependents();
+  griddep_wait();
+
+  // ---- group tables: unpadded / padded rows, tiles per group ----
+  if (warp == 0) {
+    // padded starts: exclusive scan of the counts rounded up to 64
+    const int per = (G + 31) / 32;
+    int loc = 0;
+    for (int i = 0; i < per; ++i) {
+      const int g = lane * per + i;
+      if (g < p.E) {
+        const int a = p.offsets[g], b = p.offsets[g + 1];
+        ctl.row0[g] = a;
+        ctl.nrows[g] = b - a;
+        ctl.pnrows[g] = (b - a + 63) & ~63;
+        loc += ctl.pnrows[g];
+      } else if (g < G) {
+        ctl.row0[g] = 0;
+        ctl.nrows[g] = p.T_shared;
+        ctl.pnrows[g] = p.T_shared;
+      }
+    }
+    int incl = loc;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int run = incl - loc;
+    for (int i = 0; i < per; ++i) {
+      const int g = lane * per + i;
+      if (g < p.E) {
+        ctl.prow0[g] = run;
+        run += ctl.pnrows[g];
+      } else if (g < G) {
+        ctl.prow0[g] = p.S_pad;
+      }
+    }
+    __syncwarp();
+    // tiles per group
+    int tl = 0;
+    for (int i = 0; i < per; ++i) {
+      const int g = lane * per + i;
+      if (g < G)
+        tl += Tr::row_tiles ? ((ctl.pnrows[g] + kTileM - 1) / kTileM) * ntn : nmt * ntn;
+    }
+    int tincl = tl;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, tincl, off);
+      if (lane >= off) tincl += v;
+    }
+    int trun = tincl - tl;
+    for (int i = 0; i < per; ++i) {
+      const int g = lane * per + i;
+      if (g < G) {
+        ctl.tile_prefix[g] = trun;
+        trun += Tr::row_tiles ? ((ctl.pnrows[g] + kTileM - 1) / kTileM) * ntn : nmt * ntn;
+      }
+    }
+    if (lane == 31) {
+      ctl.tile_prefix[G] = tincl;
+      ctl.total_tiles = tincl;
+    }
+  }
+  cluster_sync_all();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = ctl.tmem_base;
+  const int total = ctl.total_tiles;
+  volatile int* abort_flag = &ctl.abort;
+  unsigned int* dev_err = p.dev_err;
+
+  // k-blocks of a tile of group g
+  auto tile_kblocks = [&](int g) -> int {
+    if (Tr::row_tiles) return p.K / kBK;
+    return (ctl.pnrows[g] + kBK - 1) / kBK;
+  };
+
+  if (warp == 0) {
+    // ===================== TMA producer (lane 0 of both CTAs) =====================
+    if (lane == 0) {
+      const uint64_t pol_a = l2_policy_evict_normal();
+      const uint64_t pol_b = Tr::row_tiles ? l2_policy_evict_last() : l2_policy_evict_normal();
+      const uint32_t pair_tx = 2u * static_cast<uint32_t>(kStageBytes);
+      int stage = 0;
+      uint32_t phase = 0;
+      int g = 0, issued = 0;
+      bool ok = true;
+      for (int tile = pair; tile < total && ok; tile += npairs) {
+        while (tile >= ctl.tile_prefix[g + 1]) ++g;
+        const int local = tile - ctl.tile_prefix[g];
+        const int m = local / ntn, n = local - m * ntn;
+        const bool routed = g < p.E;
+        const int nkb = tile_kblocks(g);
+        const CUtensorMap* mA = routed ? &mapA : &mapA_sh;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_cluster(smem_u32(&ctl.empty[stage]), phase ^ 1u, abort_flag, dev_err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_leader = map_to_cta(smem_u32(&ctl.full[stage]), 0);
+          const uint32_t sa = smem_base + stage * kStageBytes;
+          const uint32_t sb = sa + kABytes;
+          if (leader) mbar_arrive_expect_tx(smem_u32(&ctl.full[stage]), pair_tx);
+          if (Tr::row_tiles) {
+            // A: 128 rows of this CTA, K-major
+            const int a0 = routed ? (kMode == kActBwd ? ctl.row0[g] : ctl.prow0[g]) : 0;
+            tma_load_2d_pair(sa, mA, full_leader, kb * kBK, a0 + m * kTileM + 128 * static_cast<int>(rank),
+                             pol_a);
+            if (kMode == kActBwd) {
+              // B = W1 (leader) / W3 (peer) columns of the tile, N-major
+              const CUtensorMap* mB =
+                  leader ? (routed ? &mapB0 : &mapB0_sh) : (routed ? &mapB1 : &mapB1_sh);
+              const int brow = (routed ? g * p.K : 0) + kb * kBK;
+              for (int c = 0; c < half_n / 64; ++c)
+                tma_load_2d_pair(sb + c * 8192, mB, full_leader, n * hw + c * 64, brow, pol_b);
+            } else {
+              // B^T rows of this CTA's half of the tile's columns, K-major
+              const bool second = kMode == kDgradX && kb * kBK >= p.K1;
+              const CUtensorMap* mB = second ? (routed ? &mapB1 : &mapB1_sh) : (routed ? &mapB0 : &mapB0_sh);
+              const int k0 = second ? kb * kBK - p.K1 : kb * kBK;
+              const int brow = (routed ? g * p.b_rows : 0) + n * kTileN + half_n * static_cast<int>(rank);
+              tma_load_2d_pair(sb, mB, full_leader, k0, brow, pol_b);
+            }
+          } else {
+            // kWgrad: k = rows of the group; A [rows, M] and B [rows, N] tiles, M/N-major
+            const int ak0 = routed ? (p.a_padded ? ctl.prow0[g] : ctl.row0[g]) : 0;
+            const int bk0 = routed ? ctl.prow0[g] : 0;
+            const int mcol = m * kTileM + 128 * static_cast<int>(rank);
+            for (int c = 0; c < 2; ++c)
+              tma_load_2d_pair(sa + c * 8192, mA, full_leader, mcol + c * 64, ak0 + kb * kBK, pol_a);
+            const CUtensorMap* mB = routed ? &mapB0 : &mapB0_sh;
+            const int ncol = n * kTileN + half_n * static_cast<int>(rank);
+            for (int c = 0; c < half_n / 64; ++c)
+              tma_load_2d_pair(sb + c * 8192, mB, full_leader, ncol + c * 64, bk0 + kb * kBK, pol_b);
+          }
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {
+        int st = stage;
+        uint32_t ph = phase;
+        for (int i = 0; i < kStages && i < issued; ++i) {
+          if (--st < 0) {
+            st = kStages - 1;
+            ph ^= 1u;
+          }
+          volatile int local_abort = 0;
+          mbar_wait_cluster(smem_u32(&ctl.full[st]), ph, &local_abort, dev_err);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ===================== MMA issuer (leader only) =====================
+    if (lane == 0 && leader) {
+      const uint32_t idesc = idesc_bf16_f32_ab(kTileM, kTileN, Tr::a_mn ? 1u : 0u, Tr::b_mn ? 1u : 0u);
+      int stage = 0;
+      uint32_t phase = 0;
+      int i = 0, g = 0;
+      bool ok = true;
+      for (int tile = pair; tile < total && ok; tile += npairs, ++i) {
+        while (tile >= ctl.tile_prefix[g + 1]) ++g;
+        const int nkb = tile_kblocks(g);
+        const int buf = i & 1;
+        const uint32_t tph = (i >> 1) & 1;
+        if (!mbar_wait_cluster(smem_u32(&ctl.tempty[buf]), tph ^ 1u, abort_flag, dev_err)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + buf * 256;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_cluster(smem_u32(&ctl.full[stage]), phase, abort_flag, dev_err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t sa = smem_base + stage * kStageBytes;
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t adesc = Tr::a_mn ? smem_desc_sw128(sa + kk * 2048, 8192, 1024)
+                                            : smem_desc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bdesc = Tr::b_mn ? smem_desc_sw128(sb + kk * 2048, 8192, 1024)
+                                            : smem_desc_sw128(sb + kk * 32, 16, 1024);
+            umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit_pair(smem_u32(&ctl.empty[stage]), 0x3);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair(smem_u32(&ctl.tfull[buf]), 0x3);
+      }
+      umma_commit_pair(smem_u32(&ctl.drain), 0x1);
+      volatile int local_abort = 0;
+      mbar_wait_cluster(smem_u32(&ctl.drain), 0, &local_abort, dev_err);
+    }
+    __syncwarp();
+  } else {
+    // ===================== epilogue (both CTAs) =====================
+    const int q = warp & 3;
+    const int part = (warp - 2) >> 2;
+    const int r_in_tile = 128 * static_cast<int>(rank) + q * 32 + lane;
+    const uint32_t tempty_leader0 = map_to_cta(smem_u32(&ctl.tempty[0]), 0);
+    const uint32_t tempty_leader1 = map_to_cta(smem_u32(&ctl.tempty[1]), 0);
+    uint8_t* stage_out = smem + kStages * kStageBytes + (warp - 2) * kOutBoxBytes;
+    int g = 0, i = 0;
+    for (int tile = pair; tile < total; tile += npairs, ++i) {
+      while (tile >= ctl.tile_prefix[g + 1]) ++g;
+      const int local = tile - ctl.tile_prefix[g];
+      const int m = local / ntn, n = local - m * ntn;
+      const bool routed = g < p.E;
+      const int buf = i & 1;
+      const uint32_t tph = (i >> 1) & 1;
+      const bool got = mbar_wait_cluster(smem_u32(&ctl.tfull[buf]), tph, abort_flag, dev_err);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after_sync();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * 256;
+      const int cols_per_part = hw / 2;
+      if (Tr::row_tiles) {
+        const int nvalid = ctl.pnrows[g];
+        const int orow0 = ctl.prow0[g];  // output rows (padded layout / shared rows)
+        const int row = m * kTileM + r_in_tile;
+        const bool valid = row < nvalid;
+        const int warp_row0 = m * kTileM + 128 * static_cast<int>(rank) + q * 32;
+        const bool full_box = warp_row0 + kOutBoxRows <= nvalid;
+        const int col0 = n * hw;
+        for (int cc = part * cols_per_part; cc < (part + 1) * cols_per_part; cc += kOutBoxCols) {
+          if (col0 + cc >= p.N) break;
+          if (kMode == kActBwd) {
+            uint32_t rg[32], ru[32];
+            tmem_ld_32cols(taddr + cc, rg);
+            tmem_ld_32cols(taddr + hw + cc, ru);
+            tmem_ld_wait();
+            if (!valid) continue;
+            const size_t orow = static_cast<size_t>(orow0 + row);
+            uint32_t hb[16];
+            load_bf16x32(p.hbar + orow * p.N + col0 + cc, hb);
+            uint32_t og[16], ou[16], oh[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              float gg[2], uu[2], hh[2], gb[2], ub[2], hv[2];
+              gg[0] = __uint_as_float(rg[2 * j]);
+              gg[1] = __uint_as_float(rg[2 * j + 1]);
+              uu[0] = __uint_as_float(ru[2 * j]);
+              uu[1] = __uint_as_float(ru[2 * j + 1]);
+              hh[0] = bf16_lo(hb[j]);
+              hh[1] = bf16_hi(hb[j]);
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                const float e = __expf(-gg[t]);
+                const float sig = __fdividef(1.0f, 1.0f + e);
+                const float silu = __fdividef(gg[t], 1.0f + e);  // the forward's expression
+                hv[t] = silu * uu[t];
+                // silu'(g) = sigmoid(g) (1 + g (1 - sigmoid(g)))
+                gb[t] = hh[t] * uu[t] * (sig * (1.0f + gg[t] * (1.0f - sig)));
+                ub[t] = hh[t] * silu;
+              }
+              og[j] = pack_bf16x2(gb[0], gb[1]);
+              ou[j] = pack_bf16x2(ub[0], ub[1]);
+              oh[j] = pack_bf16x2(hv[0], hv[1]);
+            }
+            store_bf16x32(p.gu + orow * (2 * p.N) + col0 + cc, og);
+            store_bf16x32(p.gu + orow * (2 * p.N) + p.N + col0 + cc, ou);
+            store_bf16x32(p.h + orow * p.N + col0 + cc, oh);
+          } else {
+            uint32_t ra[32];
+            tmem_ld_32cols(taddr + cc, ra);
+            tmem_ld_wait();
+            uint32_t packed[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              packed[j] = pack_bf16x2(__uint_as_float(ra[2 * j]), __uint_as_float(ra[2 * j + 1]));
+            if (full_box) {
+              bulk_wait_group_read0();
+              __syncwarp();
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                uint4* dst = reinterpret_cast<uint4*>(stage_out + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4));
+                *dst = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&mapC, smem_u32(stage_out), col0 + cc, orow0 + warp_row0);
+                bulk_commit_group();
+              }
+            } else if (valid) {
+              store_bf16x32(p.C + static_cast<size_t>(orow0 + row) * p.N + col0 + cc, packed);
+            }
+          }
+        }
+      } else {
+        // kWgrad: fp32 rows m * 256 + r (< M), columns n * 256 + cc (< N)
+        const int nkb = tile_kblocks(g);
+        const int row = m * kTileM + r_in_tile;
+        const bool valid = row < p.M;
+        for (int cc = part * cols_per_part; cc < (part + 1) * cols_per_part; cc += 32) {
+          const int col = n * kTileN + cc;
+          if (col >= p.N) break;
+          uint32_t ra[32];
+          tmem_ld_32cols(taddr + cc, ra);
+          tmem_ld_wait();
+          if (!valid) continue;
+          const bool second = col >= p.n_split;
+          float* base = routed ? (second ? p.w_b : p.w_a) : (second ? p.ws_b : p.ws_a);
+          const int ncols = second ? p.N - p.n_split : p.n_split;
+          const int c0 = second ? col - p.n_split : col;
+          float* dst = base + (routed ? static_cast<size_t>(g) * p.M * ncols : 0) +
+                       static_cast<size_t>(row) * ncols + c0;
+          float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            if (nkb == 0)
+              d4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+            else
+              d4[v] = make_float4(__uint_as_float(ra[4 * v]), __uint_as_float(ra[4 * v + 1]),
+                                  __uint_as_float(ra[4 * v + 2]), __uint_as_float(ra[4 * v + 3]));
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
+    }
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
+  }
+
+  tc_fence_before_sync();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+// Per-device launch state: co-resident CTA pairs per mode, error word address.
+struct BwdDevice {
+  int pairs[4] = {0, 0, 0, 0};
+  unsigned int* dev_err = nullptr;
+  bool ready = false;
+};
+BwdDevice g_bwd_dev[64];
+std::mutex g_bwd_mu;
+
+template <int kMode>
+cudaError_t mode_setup(int sms, int* pairs) {
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_bwd_kernel<kMode>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaOccupancyMaxActiveClusters(pairs, grouped_gemm_bwd_kernel<kMode>, &cfg);
+  if (e != cudaSuccess) return e;
+  return *pairs >= 1 ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
+cudaError_t bwd_setup(BwdDevice* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_bwd_mu);
+  BwdDevice& bd = g_bwd_dev[dev];
+  if (!bd.ready) {
+    int sms = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = mode_setup<kDgradW2>(sms, &bd.pairs[0])) != cudaSuccess) return e;
+    if ((e = mode_setup<kActBwd>(sms, &bd.pairs[1])) != cudaSuccess) return e;
+    if ((e = mode_setup<kDgradX>(sms, &bd.pairs[2])) != cudaSuccess) return e;
+    if ((e = mode_setup<kWgrad>(sms, &bd.pairs[3])) != cudaSuccess) return e;
+    if ((e = device_error_address(&bd.dev_err)) != cudaSuccess) return e;
+    bd.ready = true;
+  }
+  *out = bd;
+  return cudaSuccess;
+}
+
+template <int kMode>
+cudaError_t launch_mode(const CUtensorMap (&m)[7], BwdArgs a, cudaStream_t s, bool pdl) {
+  BwdDevice bd;
+  cudaError_t e = bwd_setup(&bd);
+  if (e != cudaSuccess) return e;
+  a.dev_err = bd.dev_err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * bd.pairs[kMode], 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  e = cudaLaunchKernelEx(&cfg, grouped_gemm_bwd_kernel<kMode>, m[0], m[1], m[2], m[3], m[4], m[5], m[6], a);
+  note_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+BwdArgs base_args(const BwdLayout& L, const int32_t* offsets) {
+  BwdArgs a = {};
+  a.offsets = offsets;
+  a.E = L.d.E;
+  a.S = L.d.T * L.d.k;
+  a.S_pad = L.S_pad;
+  a.T_shared = L.shared ? L.d.T : 0;
+  return a;
+}
+
+}  // namespace
+
+int bwd_padded_rows(const moe_dims& d) { return d.T * d.k + 64 * d.E; }
+
+cudaError_t launch_bwd_dgrad_w2(const BwdLayout& L, const int32_t* offsets, const uint16_t* ybar,
+                                const uint16_t* d_out, const uint16_t* W2, const uint16_t* Ws2,
+                                uint16_t* hbar, cudaStream_t s, bool pdl) {
+  const moe_dims& d = L.d;
+  const uint64_t rows = static_cast<uint64_t>(L.S_pad) + (L.shared ? d.T : 0);
+  CUtensorMap m[7];
+  cudaError_t e;
+  if ((e = tensor_map_2d(&m[0], ybar, L.S_pad, d.D, 128, kBK)) != cudaSuccess) return e;
+  if ((e = tensor_map_2d(&m[2], W2, static_cast<uint64_t>(d.E) * d.F, d.D, 128, kBK)) != cudaSuccess) return e;
+  if (L.shared) {
+    if ((e = tensor_map_2d(&m[1], d_out, d.T, d.D, 128, kBK)) != cudaSuccess) return e;
+    if ((e = tensor_map_2d(&m[4], Ws2, d.F, d.D, 128, kBK)) != cudaSuccess) return e;
+  } else {
+    m[1] = m[0];
+    m[4] = m[2];
+  }
+  m[3] = m[2];
+  m[5] = m[4];
+  if ((e = tensor_map_2d(&m[6], hbar, rows, d.F, kOutBoxRows, kOutBoxCols)) != cudaSuccess) return e;
+  BwdArgs a = base_args(L, offsets);
+  a.K = d.D;
+  a.N = d.F;
+  a.b_rows = d.F;
+  a.C = hbar;
+  return launch_mode<kDgradW2>(m, a, s, pdl);
+}
+
+cudaError_t launch_bwd_act(const BwdLayout& L, const int32_t* offsets, const uint16_t* x_sorted,
+                           const uint16_t* x, const uint16_t* W1, const uint16_t* W3,
+                           const uint16_t* Ws1, const uint16_t* Ws3, const uint16_t* hbar,
+                           uint16_t* gu, uint16_t* h, cudaStream_t s, bool pdl) {
+  const moe_dims& d = L.d;
+  const int S = d.T * d.k;
+  CUtensorMap m[7];
+  cudaError_t e;
+  if ((e = tensor_map_2d(&m[0], x_sorted, S, d.D, 128, kBK)) != cudaSuccess) return e;
+  if ((e = tensor_map_2d(&m[2], W1, static_cast<uint64_t>(d.E) * d.D, d.F, kBK, 64)) != cudaSuccess) return e;
+  if ((e = tensor_map_2d(&m[3], W3, static_cast<uint64_t>(d.E) * d.D, d.F, kBK, 64)) != cudaSuccess) return e;
+  if (L.shared) {
+    if ((e = tensor_map_2d(&m[1], x, d.T, d.D, 128, kBK)) != cudaSuccess) return e;
+    if ((e = tensor_map_2d(&m[4], Ws1, d.D, d.F, kBK, 64)) != cudaSuccess) return e;
+    if ((e = tensor_map_2d(&m[5], Ws3, d.D, d.F, kBK, 64)) != cudaSuccess) return e;
+  } else {
+    m[1] = m[0];
+    m[4] = m[2];
+    m[5] = m[3];
+  }
+  m[6] = m[0];  // no TMA store in this mode
+  BwdArgs a = base_args(L, offsets);
+  a.K = d.D;
+  a.N = d.F;
+  a.hbar = hbar;
+  a.gu = gu;
+  a.h = h;
+  return launch_mode<kActBwd>(m, a, s, pdl);
+}
+
+cudaError_t launch_bwd_dgrad_x(const BwdLayout& L, const int32_t* offsets, const uint16_t* gu,
+                               const uint16_t* W1, const uint16_t* W3, const uint16_t* Ws1,
+                               const uint16_t* Ws3, uint16_t* xbar, cudaStream_t s, bool pdl) {
+  const moe_dims& d = L.d;
+  const uint64_t rows = static_cast<uint64_t>(L.S_pad) + (L.shared ? d.T : 0);
+  CUtensorMap m[7];
+  cudaError_t e;
+  if ((e = tensor_map_2d(&m[0], gu, L.S_pad, 2 * d.F, 128, kBK)) != cudaSuccess) return e;
+  if ((e = tensor_map_2d(&m[2], W1, static_cast<uint64_t>(d.E) * d.D, d.F, 128, kBK)) != cudaSuccess) return e;
+  if ((e = tensor_map_2d(&m[3], W3, static_cast<uint64_t>(d.E) * d.D, d.F, 128, kBK)) != cudaSuccess) return e;
+  if (L.shared) {
+    const uint16_t* gu_sh = gu + static_cast<size_t>(L.S_pad) * 2 * d.F;
+    if ((e = tensor_map_2d(&m[1], gu_sh, d.T, 2 * d.F, 128, kBK)) != cudaSuccess) return e;
+    if ((e = tensor_map_2d(&m[4], Ws1, d.D, d.F, 128, kBK)) != cudaSuccess) return e;
+    if ((e = tensor_map_2d(&m[5], Ws3, d.D, d.F, 128, kBK)) != cudaSuccess) return e;
+  } else {
+    m[1] = m[0];
+    m[4] = m[2];
+    m[5] = m[3];
+  }
+  if ((e = tensor_map_2d(&m[6], xbar, rows, d.D, kOutBoxRows, kOutBoxCols)) != cudaSuccess) return e;
+  BwdArgs a = base_args(L, offsets);
+  a.K = 2 * d.F;
+  a.K1 = d.F;
+  a.N = d.D;
+  a.b_rows = d.D;
+  a.C = xbar;
+  return launch_mode<kDgradX>(m, a, s, pdl);
+}
+
+cudaError_t launch_bwd_wgrad(const BwdLayout& L, const int32_t* offsets, const uint16_t* A,
+                             int a_padded, int M, const uint16_t* A_sh, const uint16_t* B, int N,
+                             const uint16_t* B_sh, int n_split, float* w_a, float* w_b, float* ws_a,
+                             float* ws_b, cudaStream_t s, bool pdl) {
+  const moe_dims& d = L.d;
+  const int S = d.T * d.k;
+  CUtensorMap m[7];
+  cudaError_t e;
+  if ((e = tensor_map_2d(&m[0], A, a_padded ? L.S_pad : S, M, kBK, 64)) != cudaSuccess) return e;
+  if ((e = tensor_map_2d(&m[2], B, L.S_pad, N, kBK, 64)) != cudaSuccess) return e;
+  if (L.shared) {
+    if ((e = tensor_map_2d(&m[1], A_sh, d.T, M, kBK, 64)) != cudaSuccess) return e;
+    if ((e = tensor_map_2d(&m[4], B_sh, d.T, N, kBK, 64)) != cudaSuccess) return e;
+  } else {
+    m[1] = m[0];
+    m[4] = m[2];
+  }
+  m[3] = m[2];
+  m[5] = m[4];
+  m[6] = m[0];
+  BwdArgs a = base_args(L, offsets);
+  a.M = M;
+  a.N = N;
+  a.a_padded = a_padded;
+  a.n_split = n_split;
+  a.w_a = w_a;
+  a.w_b = w_b;
+  a.ws_a = ws_a;
+  a.ws_b = ws_b;
+  return launch_mode<kWgrad>(m, a, s, pdl);
+}
+
+}  // namespace moe

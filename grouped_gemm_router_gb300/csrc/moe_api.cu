@@ -62,6 +62,42 @@ Workspace carve(void* base, const moe_dims& d, bool shared, bool host_io) {
   return w;
 }
 
+// Backward workspace: gradient buffers in the padded sorted layout.
+struct BwdWorkspace {
+  uint16_t* ybar;  // [S_pad, D]
+  uint16_t* hbar;  // [S_pad + Tsh, F]
+  uint16_t* gu;    // [S_pad + Tsh, 2F]
+  uint16_t* h;     // [S_pad + Tsh, F]
+  uint16_t* xbar;  // [S_pad + Tsh, D]
+  float* wbar;     // [T, k]
+  float* lbar;     // [T, k]
+  float* rpart;    // router-gradient partials
+  size_t bytes;
+};
+
+BwdWorkspace carve_bwd(void* base, const moe_dims& d, bool shared) {
+  BwdWorkspace w{};
+  const size_t T = static_cast<size_t>(d.T), S = T * d.k;
+  const size_t Sp = static_cast<size_t>(bwd_padded_rows(d));
+  const size_t rows = Sp + (shared ? T : 0);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes);
+    return base ? static_cast<char*>(base) + o : nullptr;
+  };
+  w.ybar = reinterpret_cast<uint16_t*>(take(Sp * d.D * 2));
+  w.hbar = reinterpret_cast<uint16_t*>(take(rows * d.F * 2));
+  w.gu = reinterpret_cast<uint16_t*>(take(rows * d.F * 4));
+  w.h = reinterpret_cast<uint16_t*>(take(rows * d.F * 2));
+  w.xbar = reinterpret_cast<uint16_t*>(take(rows * d.D * 2));
+  w.wbar = reinterpret_cast<float*>(take(S * 4));
+  w.lbar = reinterpret_cast<float*>(take(S * 4));
+  w.rpart = reinterpret_cast<float*>(take(bwd_router_part_floats(d) * 4));
+  w.bytes = off;
+  return w;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 moe_status check_dims(const moe_dims& d) {
@@ -149,12 +185,101 @@ moe_status validate_layer(const void* x, const void* Wg, const float* bias, cons
   return MOE_OK;
 }
 
+// The backward launch sequence on validated arguments.
+moe_status run_backward(const uint16_t* x, const uint16_t* Wg, const uint16_t* W1, const uint16_t* W3,
+                        const uint16_t* W2, const uint16_t* Ws1, const uint16_t* Ws3,
+                        const uint16_t* Ws2, const uint16_t* d_out, const moe_dims& d,
+                        const Workspace& fw, const BwdWorkspace& bw, uint16_t* dx, float* dWg,
+                        float* dbias, float* dW1, float* dW3, float* dW2, float* dWs1, float* dWs3,
+                        float* dWs2, const moe_ffn_options* o, cudaStream_t s) {
+  const bool shared = Ws1 != nullptr;
+  const bool routed_in = o != nullptr && o->ids_in != nullptr;
+  const int32_t* ids = routed_in ? o->ids_in : fw.ids;
+  const float* w = routed_in ? o->weights_in : fw.w;
+  const BwdLayout L{d, shared, bwd_padded_rows(d)};
+  const size_t Sp = static_cast<size_t>(L.S_pad);
+  cudaError_t e;
+  record(o, 0, s);
+  e = launch_combine_bwd(L, d_out, fw.y, w, ids, fw.inv, fw.offsets, routed_in ? 1 : 0, bw.ybar, bw.wbar,
+                         bw.lbar, s, false);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  record(o, 1, s);
+  e = launch_bwd_dgrad_w2(L, fw.offsets, bw.ybar, d_out, W2, Ws2, bw.hbar, s, true);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  record(o, 2, s);
+  e = launch_bwd_act(L, fw.offsets, fw.x_sorted, x, W1, W3, Ws1, Ws3, bw.hbar, bw.gu, bw.h, s, true);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  record(o, 3, s);
+  e = launch_bwd_dgrad_x(L, fw.offsets, bw.gu, W1, W3, Ws1, Ws3, bw.xbar, s, true);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  record(o, 4, s);
+  e = launch_bwd_wgrad(L, fw.offsets, fw.x_sorted, 0, d.D, x, bw.gu, 2 * d.F, bw.gu + Sp * 2 * d.F, d.F,
+                       dW1, dW3, dWs1, dWs3, s, true);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_bwd_wgrad(L, fw.offsets, bw.h, 1, d.F, bw.h + Sp * d.F, bw.ybar, d.D, d_out, d.D, dW2,
+                       nullptr, dWs2, nullptr, s, true);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  record(o, 5, s);
+  e = launch_dx_gather(L, bw.xbar, ids, fw.inv, fw.offsets, routed_in ? nullptr : bw.lbar, Wg, dx, s,
+                       true);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  record(o, 6, s);
+  if (!routed_in && (dWg != nullptr || dbias != nullptr)) {
+    e = launch_router_bwd(L, x, ids, bw.lbar, bw.rpart, dWg, dbias, s, true);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  record(o, 7, s);
+  return MOE_OK;
+}
+
 }  // namespace
 }  // namespace moe
 
 using namespace moe;
 
 extern "C" {
+
+size_t moe_ffn_backward_workspace_size(moe_dims d, int has_shared) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return carve_bwd(nullptr, d, has_shared != 0).bytes;
+}
+
+moe_status moe_ffn_backward(const void* x, const void* Wg, const void* W1, const void* W3,
+                            const void* W2, const void* Ws1, const void* Ws3, const void* Ws2,
+                            const void* d_out, moe_dims d, const void* fwd_workspace,
+                            size_t fwd_ws_bytes, void* dx, float* dWg, float* dbias, float* dW1,
+                            float* dW3, float* dW2, float* dWs1, float* dWs3, float* dWs2,
+                            void* workspace, size_t ws_bytes, const moe_ffn_options* opts,
+                            void* stream) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (!x || !Wg || !W1 || !W3 || !W2 || !d_out || !fwd_workspace || !dx || !dW1 || !dW3 || !dW2 ||
+      !workspace)
+    return MOE_ERR_INVALID_ARG;
+  const int sh = shared_state(Ws1, Ws3, Ws2);
+  const int shg = shared_state(dWs1, dWs3, dWs2);
+  if (sh < 0 || shg < 0 || sh != shg) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, Wg, W1, W3, W2, Ws1, Ws3, Ws2, d_out, fwd_workspace, dx, dWg, dbias,
+                        dW1, dW3, dW2, dWs1, dWs3, dWs2, workspace};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (opts != nullptr && ((opts->ids_in == nullptr) != (opts->weights_in == nullptr)))
+    return MOE_ERR_INVALID_ARG;
+  if (opts != nullptr && opts->flags != 0) return MOE_ERR_INVALID_ARG;
+  const bool shared = sh == 1;
+  const Workspace fw = carve(const_cast<void*>(fwd_workspace), d, shared, false);
+  if (fwd_ws_bytes < fw.bytes) return MOE_ERR_WORKSPACE;
+  const BwdWorkspace bw = carve_bwd(workspace, d, shared);
+  if (ws_bytes < bw.bytes) return MOE_ERR_WORKSPACE;
+  if (d.T == 0) return MOE_OK;
+  return run_backward(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(Wg),
+                      static_cast<const uint16_t*>(W1), static_cast<const uint16_t*>(W3),
+                      static_cast<const uint16_t*>(W2), static_cast<const uint16_t*>(Ws1),
+                      static_cast<const uint16_t*>(Ws3), static_cast<const uint16_t*>(Ws2),
+                      static_cast<const uint16_t*>(d_out), d, fw, bw, static_cast<uint16_t*>(dx),
+                      dWg, dbias, dW1, dW3, dW2, dWs1, dWs3, dWs2, opts,
+                      static_cast<cudaStream_t>(stream));
+}
 
 size_t moe_ffn_workspace_size(moe_dims d, int has_shared, int host_io) {
   if (check_dims(d) != MOE_OK) return 0;

@@ -356,6 +356,12 @@ MOE_DEV uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, uint32_t b_mn_major) {
   return d;
 }
 
+// As idesc_bf16_f32 with the major-ness of A chosen too: A K-major
+// (a_mn_major = 0) or M-major (1, the transpose of a row-major [K, M] tile).
+MOE_DEV uint32_t idesc_bf16_f32_ab(uint32_t M, uint32_t N, uint32_t a_mn_major, uint32_t b_mn_major) {
+  return idesc_bf16_f32(M, N, b_mn_major) | (a_mn_major << 15);
+}
+
 // ---------------------------------------------------------------------------
 // Small helpers
 // ---------------------------------------------------------------------------

@@ -74,6 +74,51 @@ cudaError_t launch_chained_ffn(const uint16_t* x_sorted, const uint16_t* x, cons
                                const uint16_t* Ws3, const uint16_t* Ws2, const int32_t* offsets,
                                const moe_dims& d, uint16_t* y, cudaStream_t s, bool pdl = false);
 
+// ---- backward (grouped_gemm_bwd.cu, backward.cu) ----
+// Padded sorted layout of the gradient buffers: group e at rows
+// [prow0_e, prow0_e + round_up(n_e, 64)), the shared group at rows
+// [S_pad, S_pad + T).
+struct BwdLayout {
+  moe_dims d;
+  bool shared;
+  int S_pad;  // bwd_padded_rows(d)
+};
+int bwd_padded_rows(const moe_dims& d);
+// h_bar = y_bar W2^T per group (shared: d_out Ws2^T).
+cudaError_t launch_bwd_dgrad_w2(const BwdLayout& L, const int32_t* offsets, const uint16_t* ybar,
+                                const uint16_t* d_out, const uint16_t* W2, const uint16_t* Ws2,
+                                uint16_t* hbar, cudaStream_t s, bool pdl);
+// Recomputes g, u and writes g_bar | u_bar [rows, 2F] and h [rows, F].
+cudaError_t launch_bwd_act(const BwdLayout& L, const int32_t* offsets, const uint16_t* x_sorted,
+                           const uint16_t* x, const uint16_t* W1, const uint16_t* W3,
+                           const uint16_t* Ws1, const uint16_t* Ws3, const uint16_t* hbar,
+                           uint16_t* gu, uint16_t* h, cudaStream_t s, bool pdl);
+// x_bar = g_bar W1^T + u_bar W3^T per group.
+cudaError_t launch_bwd_dgrad_x(const BwdLayout& L, const int32_t* offsets, const uint16_t* gu,
+                               const uint16_t* W1, const uint16_t* W3, const uint16_t* Ws1,
+                               const uint16_t* Ws3, uint16_t* xbar, cudaStream_t s, bool pdl);
+// C[e] = A[rows_e]^T B[rows_e] in fp32, columns [0, n_split) to w_a, the rest to w_b.
+cudaError_t launch_bwd_wgrad(const BwdLayout& L, const int32_t* offsets, const uint16_t* A,
+                             int a_padded, int M, const uint16_t* A_sh, const uint16_t* B, int N,
+                             const uint16_t* B_sh, int n_split, float* w_a, float* w_b, float* ws_a,
+                             float* ws_b, cudaStream_t s, bool pdl);
+// Combine backward: y_bar (padded layout, padding rows zeroed), the gradient of
+// the gate weights and of the selected logits (zero when routed_in).
+cudaError_t launch_combine_bwd(const BwdLayout& L, const uint16_t* d_out, const uint16_t* y,
+                               const float* w, const int32_t* ids, const int32_t* inv,
+                               const int32_t* offsets, int routed_in, uint16_t* ybar, float* wbar,
+                               float* lbar, cudaStream_t s, bool pdl);
+// dx[t] = sum_j x_bar[slot j] (+ x_bar[shared row]) + sum_j lbar[t,j] Wg[:, ids[t,j]].
+cudaError_t launch_dx_gather(const BwdLayout& L, const uint16_t* xbar, const int32_t* ids,
+                             const int32_t* inv, const int32_t* offsets, const float* lbar,
+                             const uint16_t* Wg, uint16_t* dx, cudaStream_t s, bool pdl);
+// dWg = x^T logits_bar and dbias = column sums of logits_bar, via per-chunk
+// partials (deterministic); `part` holds bwd_router_part_floats(d) floats.
+size_t bwd_router_part_floats(const moe_dims& d);
+cudaError_t launch_router_bwd(const BwdLayout& L, const uint16_t* x, const int32_t* ids,
+                              const float* lbar, float* part, float* dWg, float* dbias,
+                              cudaStream_t s, bool pdl);
+
 // 2-D bf16 TMA descriptor of a row-major [rows, cols] matrix with a
 // {box_cols, box_rows} box: 128-byte swizzle (64-byte for 32-column boxes),
 // zero fill outside the tensor (grouped_gemm.cu).

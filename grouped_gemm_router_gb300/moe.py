@@ -150,6 +150,85 @@ def moe_ffn_forward_host(x_host, Wg, W1, W3, W2, k, out_host, workspace: Workspa
     return out_host
 
 
+class BackwardWorkspace:
+    """Device workspace of moe_ffn_backward, with typed views of its regions
+    (the layout documented in moe_ffn.h: padded sorted rows, the shared rows
+    from S_pad = T*k + 64*E)."""
+
+    def __init__(self, T, D, F, E, k, shared, device=None):
+        self.dims = (T, D, F, E, k)
+        self.shared = bool(shared)
+        self.nbytes = int(lib.moe_ffn_backward_workspace_size(N.dims(T, D, F, E, k), int(bool(shared))))
+        if self.nbytes == 0 and T > 0:
+            raise N.MoeError(N.MOE_ERR_UNSUPPORTED_SHAPE, "moe_ffn_backward_workspace_size")
+        self.buf = torch.empty(max(self.nbytes, 256), dtype=torch.uint8, device=device or "cuda")
+
+    def views(self):
+        T, D, F, E, k = self.dims
+        S = T * k
+        Sp = S + 64 * E
+        rows = Sp + (T if self.shared else 0)
+        out, off = {"S_pad": Sp}, 0
+
+        def take(name, n, dtype, shape):
+            nonlocal off
+            size = n * torch.tensor([], dtype=dtype).element_size()
+            out[name] = self.buf[off:off + size].view(dtype).view(*shape)
+            off += (size + 255) // 256 * 256
+
+        take("ybar", Sp * D, torch.bfloat16, (Sp, D))
+        take("hbar", rows * F, torch.bfloat16, (rows, F))
+        take("gu", rows * 2 * F, torch.bfloat16, (rows, 2 * F))
+        take("h", rows * F, torch.bfloat16, (rows, F))
+        take("xbar", rows * D, torch.bfloat16, (rows, D))
+        take("wbar", S, torch.float32, (T, k))
+        take("lbar", S, torch.float32, (T, k))
+        return out
+
+
+def padded_rows(counts):
+    """Row of each sorted position in the backward's padded layout: group e
+    starts at the sum of the earlier group sizes rounded up to 64."""
+    counts = [int(c) for c in counts]
+    prow0, run = [], 0
+    for c in counts:
+        prow0.append(run)
+        run += (c + 63) // 64 * 64
+    idx = []
+    for e, c in enumerate(counts):
+        idx.extend(range(prow0[e], prow0[e] + c))
+    return idx
+
+
+def moe_ffn_backward(x, Wg, W1, W3, W2, k, d_out, workspace: Workspace, Ws1=None, Ws3=None, Ws2=None,
+                     bwd_workspace: BackwardWorkspace | None = None, ids_in=None, weights_in=None,
+                     router=True, stage_events=None):
+    """Gradients of sum(d_out * out) for the forward call that filled
+    `workspace`.  Returns dict(dx bf16 [T, D], dW1, dW3 [E, D, F], dW2 [E, F, D]
+    (+ dWs1, dWs3, dWs2), and with router=True dWg [D, E], dbias [E]) fp32."""
+    T, D, F, E, k = layer_dims(x, W1, k)
+    shared = Ws1 is not None
+    _need(d_out, "d_out", torch.bfloat16, (T, D))
+    dev = x.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = dict(dx=torch.empty(T, D, dtype=torch.bfloat16, device=dev),
+             dW1=torch.empty(E, D, F, **f32), dW3=torch.empty(E, D, F, **f32), dW2=torch.empty(E, F, D, **f32))
+    if shared:
+        g.update(dWs1=torch.empty(D, F, **f32), dWs3=torch.empty(D, F, **f32), dWs2=torch.empty(F, D, **f32))
+    if router:
+        g.update(dWg=torch.empty(D, E, **f32), dbias=torch.empty(E, **f32))
+    if bwd_workspace is None:
+        bwd_workspace = BackwardWorkspace(T, D, F, E, k, shared, device=dev)
+    st = lib.moe_ffn_backward(_ptr(x), _ptr(Wg), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(Ws1), _ptr(Ws3), _ptr(Ws2),
+                              _ptr(d_out), N.dims(T, D, F, E, k), _ptr(workspace.buf), workspace.nbytes,
+                              _ptr(g["dx"]), _ptr(g.get("dWg")), _ptr(g.get("dbias")), _ptr(g["dW1"]),
+                              _ptr(g["dW3"]), _ptr(g["dW2"]), _ptr(g.get("dWs1")), _ptr(g.get("dWs3")),
+                              _ptr(g.get("dWs2")), _ptr(bwd_workspace.buf), bwd_workspace.nbytes,
+                              _options(stage_events, ids_in, weights_in), _stream())
+    check(st, "moe_ffn_backward")
+    return g
+
+
 def moe_route(x, Wg, k, bias=None):
     """Router GEMM + top-k + softmax -> (ids [T,k] int32, weights [T,k] fp32,
     block_hist [ceil(T/TB), E] int32 with TB = moe_route_block_tokens(T))."""

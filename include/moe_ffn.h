@@ -127,6 +127,52 @@ moe_status moe_ffn_forward_host(const void* x_host, const void* Wg, const float*
                                 moe_dims d, void* out_host, void* workspace, size_t ws_bytes,
                                 const moe_ffn_options* opts, void* stream);
 
+/* ---- Backward pass ---------------------------------------------------- */
+
+/* Bytes of device workspace moe_ffn_backward needs.  With S_pad =
+ * T*k + 64*E and R = S_pad (+T with the shared expert) it holds, each
+ * 256-byte aligned: y_bar [S_pad, D], h_bar [R, F], g_bar|u_bar [R, 2F],
+ * h [R, F], x_bar [R, D] (bf16, the routed rows of each expert padded to a
+ * multiple of 64 rows in expert order, the shared rows from S_pad), the
+ * gate-weight and selected-logit gradients [T, k] fp32 and the router-
+ * gradient partials (ceil(T/256) * (D*E + E) fp32).  0 for unsupported
+ * dimensions. */
+size_t moe_ffn_backward_workspace_size(moe_dims d, int has_shared);
+
+/* Gradients of L = sum(d_out * out) for the layer moe_ffn_forward computed
+ * ("Triton MoE Kernels & Memory Checkpointing", Part A, section 8: the
+ * SwiGLU expert's gradients -- h_bar split into g_bar = h_bar*u*silu'(g) and
+ * u_bar = h_bar*silu(g), x_bar = g_bar W1^T + u_bar W3^T, the weight
+ * gradients as outer products -- written as hand-made kernels; and the chain
+ * rule through the combine, softmax and router of "Chinchilla scaling, MoE,
+ * and fused Triton kernels", section "PyTorch MoE implementation").
+ *   Inputs: the forward's x, Wg, W1, W3, W2, Ws1..Ws2 (as moe_ffn_forward) and
+ *   d_out [T, D] bf16, plus the forward's workspace (fwd_workspace,
+ *   fwd_ws_bytes >= moe_ffn_workspace_size(d, has_shared, 0)) holding the
+ *   routing, permutation, x_sorted and y of that forward call; it is read
+ *   only.  g and u are recomputed (the activations are not stored).
+ *   Outputs: dx [T, D] bf16; dW1, dW3 [E, D, F], dW2 [E, F, D] and, with the
+ *   shared expert, dWs1, dWs3 [D, F], dWs2 [F, D] in fp32 (all written, zero
+ *   for an expert with no tokens); dWg [D, E] and dbias [E] fp32 (each may be
+ *   NULL to skip).  Top-k is piecewise constant: unselected logits get no
+ *   gradient.
+ *   opts (nullable): ids_in / weights_in must repeat the fixed routing the
+ *   forward was given, and then the router gets no gradient (dWg, dbias and
+ *   the router term of dx are zero / skipped); stage_events [0..7] are
+ *   recorded before the combine backward, after it, after h_bar, after
+ *   g_bar|u_bar, after x_bar, after the weight gradients, after dx and after
+ *   the router gradient; flags must be 0.
+ *   Precision: fp32 accumulation everywhere; y_bar, h_bar, g_bar, u_bar, h
+ *   and x_bar are stored as bf16 between the GEMMs; dx is summed in fp32 and
+ *   rounded once.  Deterministic (no atomics). */
+moe_status moe_ffn_backward(const void* x, const void* Wg, const void* W1, const void* W3,
+                            const void* W2, const void* Ws1, const void* Ws3, const void* Ws2,
+                            const void* d_out, moe_dims d, const void* fwd_workspace,
+                            size_t fwd_ws_bytes, void* dx, float* dWg, float* dbias, float* dW1,
+                            float* dW3, float* dW2, float* dWs1, float* dWs3, float* dWs2,
+                            void* workspace, size_t ws_bytes, const moe_ffn_options* opts,
+                            void* stream);
+
 /* ---- Stage entry points (the same kernels moe_ffn_forward launches) ---- */
 
 /* Scratch bytes moe_route needs: the router weights repacked in the MMA

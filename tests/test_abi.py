@@ -98,6 +98,45 @@ def test_argument_validation_before_launch(native):
     assert N.lib.moe_launch_count() == 0
 
 
+def test_backward_argument_validation_before_launch(native):
+    N = native
+    p = ctypes.c_void_p
+    good = N.dims(256, 128, 256, 4, 2)
+    fws = N.lib.moe_ffn_workspace_size(good, 0, 0)
+    bws = N.lib.moe_ffn_backward_workspace_size(good, 0)
+
+    def bwd_call(d=good, d_out=FAKE, fwd_bytes=fws, ws_bytes=bws, shared=(None, None, None),
+                 dshared=(None, None, None), opts=None):
+        ptr = lambda v: p(v) if v else None
+        return N.lib.moe_ffn_backward(p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), *map(ptr, shared),
+                                      ptr(d_out), d, p(FAKE), fwd_bytes, p(FAKE), None, None, p(FAKE), p(FAKE),
+                                      p(FAKE), *map(ptr, dshared), p(FAKE), ws_bytes,
+                                      ctypes.byref(opts) if opts else None, None)
+
+    assert bwd_call(d=N.dims(0, 128, 256, 4, 2)) == N.MOE_OK              # nothing to do
+    assert bwd_call(d_out=0) == N.MOE_ERR_INVALID_ARG                     # no incoming gradient
+    assert bwd_call(shared=(FAKE, FAKE, FAKE)) == N.MOE_ERR_INVALID_ARG   # shared weights, no gradients
+    assert bwd_call(dshared=(FAKE, FAKE, FAKE)) == N.MOE_ERR_INVALID_ARG  # gradients, no shared weights
+    assert bwd_call(fwd_bytes=fws - 1) == N.MOE_ERR_WORKSPACE
+    assert bwd_call(ws_bytes=bws - 1) == N.MOE_ERR_WORKSPACE
+    assert bwd_call(d=N.dims(256, 100, 256, 4, 2)) == N.MOE_ERR_UNSUPPORTED_SHAPE
+    o = N.MoeOptions()
+    o.flags = N.MOE_FFN_CHAINED
+    assert bwd_call(opts=o) == N.MOE_ERR_INVALID_ARG                      # no flags in the backward
+    assert N.lib.moe_launch_count() == 0
+
+
+def test_backward_workspace_size_matches_documented_layout(native):
+    a = lambda n: (n + 255) // 256 * 256
+    for T, D, F, E, k, sh in [(256, 128, 256, 4, 2, 0), (32768, 768, 1536, 8, 2, 1), (1, 64, 64, 1, 1, 1)]:
+        S = T * k
+        Sp = S + 64 * E
+        R = Sp + (T if sh else 0)
+        n = a(Sp * D * 2) + a(R * F * 2) + a(R * F * 4) + a(R * F * 2) + a(R * D * 2) + 2 * a(S * 4)
+        n += a(((T + 255) // 256) * (D * E + E) * 4)
+        assert native.lib.moe_ffn_backward_workspace_size(native.dims(T, D, F, E, k), sh) == n
+
+
 def test_workspace_size_matches_documented_layout(native):
     def layout(T, D, F, E, k, shared, host_io):
         a = lambda n: (n + 255) // 256 * 256
