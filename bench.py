@@ -357,6 +357,78 @@ def run_chain_sweep(args):
         del G, ws
 
 
+def run_backward_bench(args, w):
+    """Training step of the layer: forward then backward (d_out synthetic),
+    L2 flushed before each step.  One JSON line: tokens/s of forward +
+    backward, the backward's stage times and each backward GEMM's rate."""
+    import torch
+    from grouped_gemm_router_gb300 import build
+    build.build()
+    from grouped_gemm_router_gb300 import moe
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pk, pk_kind = peaks()
+    L = inputs.make_layer(w)
+    G = {key: to_dev(v, dev) for key, v in L.items()}
+    T, D, F, E, k = w.T, w.D, w.F, w.E, w.k
+    rng = np.random.default_rng(1)
+    d_out = to_dev(inputs.f32_to_bf16_bits(rng.standard_normal((T, D)).astype(np.float32)), dev)
+    ws = moe.Workspace(T, D, F, E, k, w.shared, device=dev)
+    bws = moe.BackwardWorkspace(T, D, F, E, k, w.shared, device=dev)
+    out = torch.empty(T, D, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+    sh = dict(Ws1=G["Ws1"], Ws3=G["Ws3"], Ws2=G["Ws2"]) if w.shared else {}
+
+    def step(fev=None, bev=None):
+        moe.moe_ffn_forward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], k, bias=G["bias"], out=out,
+                            workspace=ws, stage_events=fev, **sh)
+        return moe.moe_ffn_backward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], k, d_out, ws,
+                                    bwd_workspace=bws, stage_events=bev, **sh)
+
+    nb = max(args.steps, 1)
+    fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(nb)]
+    bevs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(nb)]
+    for row in fevs + bevs:
+        for ev in row:
+            ev.record()
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    with ClockSampler(0) as cs:
+        for i in range(nb):
+            flush.fill_(1.0)
+            sink.copy_(flush.sum())
+            step(fevs[i], bevs[i])
+        torch.cuda.synchronize()
+        clocks = cs.stop()
+    assert moe.device_error() == 0
+    mean = lambda evs, a, b: float(np.mean([e[a].elapsed_time(e[b]) for e in evs])) / 1e3
+    fwd_s = mean(fevs, 0, 5)
+    bwd_s = mean(bevs, 0, 7)
+    R = T * k + (T if w.shared else 0)
+    names = ["combine_bwd", "w2_dgrad", "swiglu_bwd_recompute", "x_dgrad", "wgrad_w1w3_w2", "dx_gather",
+             "router_bwd"]
+    stage = {n: mean(bevs, i, i + 1) * 1e3 for i, n in enumerate(names)}
+    flops = {"w2_dgrad": 2 * R * D * F, "swiglu_bwd_recompute": 4 * R * D * F, "x_dgrad": 4 * R * D * F,
+             "wgrad_w1w3_w2": 6 * R * D * F}
+    bwd_flops = sum(flops.values()) + 2 * T * D * E
+    line = {"metric": "MoE FFN forward + backward tokens/s on 1 GB300", "value": T / (fwd_s + bwd_s),
+            "unit": "tokens/s", "steps": nb, "warmup": max(args.warmup, 3), "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": w.name, "T": T, "D": D, "F": F, "E": E, "k": k,
+                                            "shared_expert": w.shared,
+                                            "l2": "flushed before each step (512 MB write + read back)"},
+            "fwd_ms": fwd_s * 1e3, "bwd_ms": bwd_s * 1e3,
+            "fwd_tflops": active_flops(w) / fwd_s / 1e12, "bwd_tflops": bwd_flops / bwd_s / 1e12,
+            "bwd_stage_ms": stage,
+            "bwd_gemm_frac_of_bf16_peak": {n: f / (stage[n] / 1e3) / 1e12 / pk["bf16_tflops"]
+                                           for n, f in flops.items()},
+            "peak": {"bf16_tflops": pk["bf16_tflops"], "kind": pk_kind}, "clocks": clocks,
+            "bwd_launches_per_step": 9}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -370,7 +442,12 @@ def main():
                          "'chained': chained vs unchained expert FFN (D <= 256)")
     ap.add_argument("--chain-shape", default=None, metavar="TxDxF",
                     help="with --sweep chained: measure this one shape only")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the training step (forward + backward) instead of the forward")
     args = ap.parse_args()
+    if args.backward:
+        run_backward_bench(args, inputs.WORKLOADS[args.workload])
+        return
     if args.sweep == "chained":
         run_chain_sweep(args)
         return
