@@ -389,7 +389,7 @@ def run_backward_bench(args, w):
 
     nb = max(args.steps, 1)
     fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(nb)]
-    bevs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(nb)]
+    bevs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(nb)]
     for row in fevs + bevs:
         for ev in row:
             ev.record()
@@ -406,13 +406,13 @@ def run_backward_bench(args, w):
     assert moe.device_error() == 0
     mean = lambda evs, a, b: float(np.mean([e[a].elapsed_time(e[b]) for e in evs])) / 1e3
     fwd_s = mean(fevs, 0, 5)
-    bwd_s = mean(bevs, 0, 7)
+    bwd_s = mean(bevs, 0, 8)
     R = T * k + (T if w.shared else 0)
-    names = ["combine_bwd", "w2_dgrad", "swiglu_bwd_recompute", "x_dgrad", "wgrad_w1w3_w2", "dx_gather",
-             "router_bwd"]
+    names = ["combine_bwd", "w2_dgrad", "swiglu_bwd_recompute", "x_dgrad", "wgrad_w1w3", "wgrad_w2",
+             "dx_gather", "router_bwd"]
     stage = {n: mean(bevs, i, i + 1) * 1e3 for i, n in enumerate(names)}
     flops = {"w2_dgrad": 2 * R * D * F, "swiglu_bwd_recompute": 4 * R * D * F, "x_dgrad": 4 * R * D * F,
-             "wgrad_w1w3_w2": 6 * R * D * F}
+             "wgrad_w1w3": 4 * R * D * F, "wgrad_w2": 2 * R * D * F}
     bwd_flops = sum(flops.values()) + 2 * T * D * E
     line = {"metric": "MoE FFN forward + backward tokens/s on 1 GB300", "value": T / (fwd_s + bwd_s),
             "unit": "tokens/s", "steps": nb, "warmup": max(args.warmup, 3), "dtype": "bf16",

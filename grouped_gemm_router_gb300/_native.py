@@ -34,7 +34,7 @@ class MoeDims(ctypes.Structure):
 
 
 class MoeOptions(ctypes.Structure):
-    _fields_ = [("stage_events", ctypes.c_void_p * 8),
+    _fields_ = [("stage_events", ctypes.c_void_p * 12),
                 ("ids_in", ctypes.c_void_p),
                 ("weights_in", ctypes.c_void_p),
                 ("flags", ctypes.c_uint32)]

@@ -9,6 +9,8 @@
 //   l_bar[t,j]  = w[t,j] (w_bar[t,j] - sum_i w[t,i] w_bar[t,i])   (softmax)
 //   dx[t]       = sum_j x_bar[slot j] (+ shared x_bar[t]) + sum_j l_bar[t,j] Wg[:, ids[t,j]]
 //   dWg         = x^T l_bar (scattered to the selected experts),  dbias = sum_t l_bar
+//                 (computed over the sorted rows: dWg[:, e] = sum over expert e's rows of
+//                 l_bar x_sorted)
 // All are gathers with fixed summation orders (no atomics), so the results
 // are deterministic.  Top-k itself is piecewise constant: unselected logits
 // get no gradient.
@@ -21,8 +23,6 @@ namespace {
 
 constexpr int kBwdThreads = 256;
 constexpr int kBwdWarps = kBwdThreads / 32;
-constexpr int kRouterTokens = 256;  // tokens per router-gradient partial
-constexpr int kRouterCols = 64;     // x columns per router-gradient block
 
 // prow0[e] (e <= E): exclusive prefix sum of the group sizes rounded up to 64.
 MOE_DEV void padded_starts(const int32_t* offsets, int E, int* prow0) {
@@ -65,10 +65,17 @@ __global__ void __launch_bounds__(kBwdThreads) combine_bwd_kernel(
     const uint4* __restrict__ d_out, const uint4* __restrict__ y, const float* __restrict__ w,
     const int32_t* __restrict__ ids, const int32_t* __restrict__ inv,
     const int32_t* __restrict__ offsets, int E, int T, int k, int D, int routed_in,
-    uint4* __restrict__ ybar, float* __restrict__ wbar, float* __restrict__ lbar) {
+    uint4* __restrict__ ybar, float* __restrict__ wbar, float* __restrict__ lbar,
+    const uint16_t* __restrict__ Wg, uint16_t* __restrict__ wgt) {
   __shared__ int prow0[MOE_MAX_EXPERTS + 1];
   griddep_wait();
   griddep_launch_dependents();
+  // Wg^T [E, D] for the router term of dx (contiguous rows per expert)
+  if (!routed_in)
+    for (int i = blockIdx.x * kBwdThreads + threadIdx.x; i < E * D; i += gridDim.x * kBwdThreads) {
+      const int e = i / D, d = i - e * D;
+      wgt[i] = Wg[static_cast<size_t>(d) * E + e];
+    }
   padded_starts(offsets, E, prow0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kBwdWarps + warp;
@@ -134,7 +141,7 @@ __global__ void __launch_bounds__(kBwdThreads) combine_bwd_kernel(
 __global__ void __launch_bounds__(kBwdThreads) dx_gather_kernel(
     const uint4* __restrict__ xbar, const int32_t* __restrict__ ids, const int32_t* __restrict__ inv,
     const int32_t* __restrict__ offsets, const float* __restrict__ lbar,
-    const uint16_t* __restrict__ Wg, int E, int T, int k, int D, int S_pad, int has_shared,
+    const uint4* __restrict__ wgt, int E, int T, int k, int D, int S_pad, int has_shared,
     uint4* __restrict__ dx) {
   __shared__ int prow0[MOE_MAX_EXPERTS + 1];
   griddep_wait();
@@ -184,10 +191,12 @@ __global__ void __launch_bounds__(kBwdThreads) dx_gather_kernel(
         const float l = __shfl_sync(0xffffffffu, my_l, j);
         const int e = __shfl_sync(0xffffffffu, my_e, j);
         if (l == 0.f) continue;
+        const uint4 v = __ldg(wgt + static_cast<size_t>(e) * n16 + c);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint16_t wv = Wg[static_cast<size_t>(c * 8 + i) * E + e];
-          acc[i] = fmaf(l, __uint_as_float(static_cast<uint32_t>(wv) << 16), acc[i]);
+        for (int q = 0; q < 4; ++q) {
+          acc[2 * q] = fmaf(l, bf16_lo(u[q]), acc[2 * q]);
+          acc[2 * q + 1] = fmaf(l, bf16_hi(u[q]), acc[2 * q + 1]);
         }
       }
     }
@@ -198,106 +207,147 @@ __global__ void __launch_bounds__(kBwdThreads) dx_gather_kernel(
   }
 }
 
-// Partial router gradients of one chunk of kRouterTokens tokens and
-// kRouterCols columns of x: part[chunk][d][e] = sum_t x[t,d] l_bar[t,e] and
-// (column block 0) part_bias[chunk][e] = sum_t l_bar[t,e].
-__global__ void __launch_bounds__(kRouterCols) router_bwd_partial_kernel(
-    const uint16_t* __restrict__ x, const int32_t* __restrict__ ids, const float* __restrict__ lbar,
-    int T, int D, int E, int k, float* __restrict__ part, float* __restrict__ part_bias) {
-  extern __shared__ float acc[];  // [E][kRouterCols]
-  __shared__ float bacc[MOE_MAX_EXPERTS];
-  griddep_wait();
-  griddep_launch_dependents();
-  const int tid = threadIdx.x;
-  const int d = blockIdx.x * kRouterCols + tid;
-  const int chunk = blockIdx.y;
-  for (int e = 0; e < E; ++e) acc[e * kRouterCols + tid] = 0.f;
-  for (int e = tid; e < E; e += kRouterCols) bacc[e] = 0.f;
-  __syncthreads();
-  const int t0 = chunk * kRouterTokens, t1 = min(t0 + kRouterTokens, T);
-  for (int t = t0; t < t1; ++t) {
-    const float xv = d < D ? __uint_as_float(static_cast<uint32_t>(x[static_cast<size_t>(t) * D + d]) << 16) : 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int e = ids[static_cast<size_t>(t) * k + j];
-      if (e < 0 || e >= E) continue;
-      const float l = lbar[static_cast<size_t>(t) * k + j];
-      acc[e * kRouterCols + tid] = fmaf(xv, l, acc[e * kRouterCols + tid]);
-      if (blockIdx.x == 0 && tid == 0) bacc[e] += l;
+// Router gradient over the sorted rows: dWg[:, e] = sum over the rows p of
+// expert e of l_bar[perm[p]] x_sorted[p, :], dbias[e] = sum of those
+// l_bar.  Rows are cut into chunks of kRouterRows that never cross a group;
+// block (chunk, column slab) writes the partial sums of its chunk, and the
+// reduce kernel adds each expert's chunks in order.
+constexpr int kRouterRows = 64;
+
+// Group and first row of global chunk `c` (chunks are numbered group by
+// group); false past the last chunk.
+MOE_DEV bool chunk_of(const int32_t* offsets, int E, int c, int* e_out, int* r0, int* r1) {
+  int base = 0;
+  for (int e = 0; e < E; ++e) {
+    const int n = offsets[e + 1] - offsets[e];
+    const int nc = (n + kRouterRows - 1) / kRouterRows;
+    if (c < base + nc) {
+      *e_out = e;
+      *r0 = offsets[e] + (c - base) * kRouterRows;
+      *r1 = min(*r0 + kRouterRows, offsets[e + 1]);
+      return true;
     }
+    base += nc;
   }
-  __syncthreads();
-  if (d < D)
-    for (int e = 0; e < E; ++e) part[(static_cast<size_t>(chunk) * D + d) * E + e] = acc[e * kRouterCols + tid];
-  if (blockIdx.x == 0)
-    for (int e = tid; e < E; e += kRouterCols) part_bias[static_cast<size_t>(chunk) * E + e] = bacc[e];
+  return false;
 }
 
-// dWg[d][e] and dbias[e]: the partials summed over the chunks in order.
+__global__ void __launch_bounds__(kBwdThreads) router_bwd_partial_kernel(
+    const uint4* __restrict__ x_sorted, const int32_t* __restrict__ perm, const float* __restrict__ lbar,
+    const int32_t* __restrict__ offsets, int E, int D, float* __restrict__ part,
+    float* __restrict__ part_bias) {
+  __shared__ float lw[kRouterRows];
+  griddep_wait();
+  griddep_launch_dependents();
+  int e, r0, r1;
+  if (!chunk_of(offsets, E, blockIdx.x, &e, &r0, &r1)) return;
+  const int n = r1 - r0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) lw[i] = lbar[perm[r0 + i]];
+  __syncthreads();
+  const int n16 = D >> 3;
+  const int c = blockIdx.y * blockDim.x + threadIdx.x;  // 8-column group
+  if (c < n16) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    const uint4* col = x_sorted + static_cast<size_t>(r0) * n16 + c;
+#pragma unroll 8
+    for (int r = 0; r < n; ++r) {
+      const uint4 v = __ldg(col + static_cast<size_t>(r) * n16);
+      const float l = lw[r];
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] = fmaf(l, bf16_lo(u[q]), acc[2 * q]);
+        acc[2 * q + 1] = fmaf(l, bf16_hi(u[q]), acc[2 * q + 1]);
+      }
+    }
+    float4* dst = reinterpret_cast<float4*>(part + static_cast<size_t>(blockIdx.x) * D + 8 * c);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+  if (blockIdx.y == 0 && threadIdx.x < 32) {
+    float sb = 0.f;
+    for (int i = threadIdx.x; i < n; i += 32) sb += lw[i];
+    sb = warp_sum(sb);
+    if (threadIdx.x == 0) part_bias[blockIdx.x] = sb;
+  }
+}
+
+// dWg[d][e] and dbias[e]: expert e's chunk partials added in chunk order.
 __global__ void router_bwd_reduce_kernel(const float* __restrict__ part, const float* __restrict__ part_bias,
-                                         int nchunks, int D, int E, float* __restrict__ dWg,
-                                         float* __restrict__ dbias) {
+                                         const int32_t* __restrict__ offsets, int D, int E,
+                                         float* __restrict__ dWg, float* __restrict__ dbias) {
   griddep_wait();
   griddep_launch_dependents();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  const int n = D * E;
-  if (i < n) {
-    if (dWg == nullptr) return;
-    float s = 0.f;
-    for (int c = 0; c < nchunks; ++c) s += part[static_cast<size_t>(c) * n + i];
+  const bool bias_item = i >= D * E;
+  if (i >= D * E + E) return;
+  const int e = bias_item ? i - D * E : i % E;
+  const int d = bias_item ? 0 : i / E;
+  int base = 0;
+  for (int g = 0; g < e; ++g)
+    base += (offsets[g + 1] - offsets[g] + kRouterRows - 1) / kRouterRows;
+  const int nc = (offsets[e + 1] - offsets[e] + kRouterRows - 1) / kRouterRows;
+  float s = 0.f;
+  for (int c = base; c < base + nc; ++c) s += bias_item ? part_bias[c] : part[static_cast<size_t>(c) * D + d];
+  if (bias_item) {
+    if (dbias != nullptr) dbias[e] = s;
+  } else if (dWg != nullptr) {
     dWg[i] = s;
-  } else if (i < n + E && dbias != nullptr) {
-    const int e = i - n;
-    float s = 0.f;
-    for (int c = 0; c < nchunks; ++c) s += part_bias[static_cast<size_t>(c) * E + e];
-    dbias[e] = s;
   }
 }
 
-int router_chunks(int T) { return (T + kRouterTokens - 1) / kRouterTokens; }
+// Upper bound of the number of group-aligned row chunks.
+int router_chunks(const moe_dims& d) { return (d.T * d.k) / kRouterRows + d.E; }
 
 }  // namespace
 
 cudaError_t launch_combine_bwd(const BwdLayout& L, const uint16_t* d_out, const uint16_t* y,
                                const float* w, const int32_t* ids, const int32_t* inv,
                                const int32_t* offsets, int routed_in, uint16_t* ybar, float* wbar,
-                               float* lbar, cudaStream_t s, bool pdl) {
+                               float* lbar, const uint16_t* Wg, uint16_t* wgt, cudaStream_t s, bool pdl) {
   const moe_dims& d = L.d;
   const int warps = d.T > 64 * d.E ? d.T : 64 * d.E;
   const dim3 grid((warps + kBwdWarps - 1) / kBwdWarps);
   return launch_kernel(combine_bwd_kernel, grid, dim3(kBwdThreads), 0, s, pdl,
                        reinterpret_cast<const uint4*>(d_out), reinterpret_cast<const uint4*>(y), w, ids,
                        inv, offsets, d.E, d.T, d.k, d.D, routed_in, reinterpret_cast<uint4*>(ybar), wbar,
-                       lbar);
+                       lbar, Wg, wgt);
 }
 
 cudaError_t launch_dx_gather(const BwdLayout& L, const uint16_t* xbar, const int32_t* ids,
                              const int32_t* inv, const int32_t* offsets, const float* lbar,
-                             const uint16_t* Wg, uint16_t* dx, cudaStream_t s, bool pdl) {
+                             const uint16_t* wgt, uint16_t* dx, cudaStream_t s, bool pdl) {
   const moe_dims& d = L.d;
   const dim3 grid((d.T + kBwdWarps - 1) / kBwdWarps);
   return launch_kernel(dx_gather_kernel, grid, dim3(kBwdThreads), 0, s, pdl,
-                       reinterpret_cast<const uint4*>(xbar), ids, inv, offsets, lbar, Wg, d.E, d.T, d.k,
-                       d.D, L.S_pad, L.shared ? 1 : 0, reinterpret_cast<uint4*>(dx));
+                       reinterpret_cast<const uint4*>(xbar), ids, inv, offsets, lbar,
+                       reinterpret_cast<const uint4*>(wgt), d.E, d.T, d.k, d.D, L.S_pad,
+                       L.shared ? 1 : 0, reinterpret_cast<uint4*>(dx));
 }
 
 size_t bwd_router_part_floats(const moe_dims& d) {
-  return static_cast<size_t>(router_chunks(d.T)) * (static_cast<size_t>(d.D) * d.E + d.E);
+  return static_cast<size_t>(router_chunks(d)) * (static_cast<size_t>(d.D) + 1);
 }
 
-cudaError_t launch_router_bwd(const BwdLayout& L, const uint16_t* x, const int32_t* ids,
-                              const float* lbar, float* part, float* dWg, float* dbias,
-                              cudaStream_t s, bool pdl) {
+cudaError_t launch_router_bwd(const BwdLayout& L, const uint16_t* x_sorted, const int32_t* perm,
+                              const int32_t* offsets, const float* lbar, float* part, float* dWg,
+                              float* dbias, cudaStream_t s, bool pdl) {
   const moe_dims& d = L.d;
-  const int nch = router_chunks(d.T);
-  float* part_bias = part + static_cast<size_t>(nch) * d.D * d.E;
-  const dim3 grid((d.D + kRouterCols - 1) / kRouterCols, nch);
-  const size_t smem = sizeof(float) * d.E * kRouterCols;
-  cudaError_t e = launch_kernel(router_bwd_partial_kernel, grid, dim3(kRouterCols), smem, s, pdl, x, ids,
-                                lbar, d.T, d.D, d.E, d.k, part, part_bias);
+  const int nch = router_chunks(d);
+  float* part_bias = part + static_cast<size_t>(nch) * d.D;
+  // one thread per 8 columns, up to 256 threads per block
+  const int n16 = d.D / 8;
+  const int threads = n16 >= kBwdThreads ? kBwdThreads : (n16 + 31) / 32 * 32;
+  const dim3 grid(nch, (n16 + threads - 1) / threads);
+  cudaError_t e = launch_kernel(router_bwd_partial_kernel, grid, dim3(threads), 0, s, pdl,
+                                reinterpret_cast<const uint4*>(x_sorted), perm, lbar, offsets, d.E, d.D,
+                                part, part_bias);
   if (e != cudaSuccess) return e;
   const int n = d.D * d.E + d.E;
   return launch_kernel(router_bwd_reduce_kernel, dim3((n + 255) / 256), dim3(256), 0, s, pdl,
-                       static_cast<const float*>(part), static_cast<const float*>(part_bias), nch, d.D,
+                       static_cast<const float*>(part), static_cast<const float*>(part_bias), offsets, d.D,
                        d.E, dWg, dbias);
 }
 

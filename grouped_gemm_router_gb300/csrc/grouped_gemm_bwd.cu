@@ -48,16 +48,28 @@ constexpr int kMaxGroups = MOE_MAX_EXPERTS + 1;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kTileM = 256;                   // rows per pair tile
 constexpr int kTileN = 256;                   // MMA N
-constexpr int kStages = 6;
+constexpr int kStages = 6;                    // stage ring (the activation mode uses 5)
 constexpr int kABytes = 128 * kBK * 2;        // 16 KB: this CTA's half of A per k-block
 constexpr int kBBytes = 128 * kBK * 2;        // 16 KB: this CTA's half of B per k-block
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kOutBoxRows = 32;
 constexpr int kOutBoxCols = 32;
 constexpr int kOutBoxBytes = kOutBoxRows * kOutBoxCols * 2;
-constexpr int kSmemBytes = kStages * kStageBytes + kEpiWarps * kOutBoxBytes + 1024;
 
 enum : int { kDgradW2 = 0, kActBwd = 1, kDgradX = 2, kWgrad = 3 };
+
+// Weight-gradient tiles differ in length (a group's rows); up to kMaxLptTiles
+// of them are assigned longest first to the least-loaded pair.
+constexpr int kMaxLptTiles = 2048;
+constexpr int kMaxMyTiles = 64;
+
+// The activation mode stages three output boxes per epilogue warp (g_bar,
+// u_bar, h) and gives up one stage of the ring for them.
+__host__ __device__ constexpr int stages_of(int mode) { return mode == kActBwd ? kStages - 1 : kStages; }
+__host__ __device__ constexpr int out_boxes_of(int mode) { return mode == kActBwd ? 3 : 1; }
+__host__ __device__ constexpr int smem_bytes_of(int mode) {
+  return stages_of(mode) * kStageBytes + kEpiWarps * out_boxes_of(mode) * kOutBoxBytes + 1024;
+}
 
 template <int kMode>
 struct Traits {
@@ -101,7 +113,10 @@ struct BwdCtl {
   uint32_t tmem_base;
   int abort;
   int total_tiles;
-  int tile_prefix[kMaxGroups + 1];
+  int tile_prefix[kMaxGroups + 1];  // by position in the tile order
+  int gorder[kMaxGroups];           // group at each position of the tile order
+  int my_count;                     // tiles of this pair in my_tiles, or -1: round robin
+  int my_tiles[kMaxMyTiles];
   int row0[kMaxGroups];   // unpadded first row (forward layout)
   int prow0[kMaxGroups];  // padded first row (shared group: S_pad)
   int nrows[kMaxGroups];
@@ -135,8 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const __grid_constant__ CUtensorMap mapB1,
                             const __grid_constant__ CUtensorMap mapB0_sh,
                             const __grid_constant__ CUtensorMap mapB1_sh,
-                            const __grid_constant__ CUtensorMap mapC, const BwdArgs p) {
+                            const __grid_constant__ CUtensorMap mapC,
+                            const __grid_constant__ CUtensorMap mapC2, const BwdArgs p) {
   using Tr = Traits<kMode>;
+  constexpr int kSt = stages_of(kMode);
   extern __shared__ uint8_t bwd_smem_raw[];
   __shared__ BwdCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -158,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&mapA);
     tma_prefetch_desc(&mapB0);
-    for (int st = 0; st < kStages; ++st) {
+    for (int st = 0; st < kSt; ++st) {
       mbar_init(smem_u32(&ctl.full[st]), 1);
       mbar_init(smem_u32(&ctl.empty[st]), 1);
     }
@@ -175,10 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish_pair();
     tc_fence_before_sync();
   }
-  griddep_launch_dependents();
-  griddep_wait();
-
-  // ---- group tables: unpadded / padded rows, tiles per group ----
+  // ---- group tables: unpadded / padded rows, tiles per group, tile order.
+  // They read only the forward's offsets, so they run before waiting for the
+  // previous kernel. ----
   if (warp == 0) {
     // padded starts: exclusive scan of the counts rounded up to 64
     const int per = (G + 31) / 32;
@@ -214,12 +230,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-    // tiles per group
+    // Tile order: group by group.  Weight-gradient tiles of the shared group
+    // reduce over all T rows (k times longer than a routed tile's rows), so
+    // they come first and the routed tiles fill in behind them.
+    // weight gradients: groups by decreasing length (ties by index), so the
+    // greedy assignment below sees the longest tiles first
+    auto kblocks_of = [&](int g) { return (ctl.pnrows[g] + kBK - 1) / kBK; };
+    if (!Tr::row_tiles) {
+      for (int i = 0; i < per; ++i) {
+        const int g = lane * per + i;
+        if (g < G) {
+          const int c = kblocks_of(g);
+          int rnk = 0;
+          for (int h = 0; h < G; ++h) {
+            const int ch = kblocks_of(h);
+            rnk += (ch > c || (ch == c && h < g)) ? 1 : 0;
+          }
+          ctl.gorder[rnk] = g;
+        }
+      }
+    } else {
+      for (int i = 0; i < per; ++i) {
+        const int g = lane * per + i;
+        if (g < G) ctl.gorder[g] = g;
+      }
+    }
+    __syncwarp();
+    auto group_at = [&](int pos) { return ctl.gorder[pos]; };
     int tl = 0;
     for (int i = 0; i < per; ++i) {
-      const int g = lane * per + i;
-      if (g < G)
+      const int pos = lane * per + i;
+      if (pos < G) {
+        const int g = group_at(pos);
         tl += Tr::row_tiles ? ((ctl.pnrows[g] + kTileM - 1) / kTileM) * ntn : nmt * ntn;
+      }
     }
     int tincl = tl;
 #pragma unroll
@@ -229,9 +273,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int trun = tincl - tl;
     for (int i = 0; i < per; ++i) {
-      const int g = lane * per + i;
-      if (g < G) {
-        ctl.tile_prefix[g] = trun;
+      const int pos = lane * per + i;
+      if (pos < G) {
+        const int g = group_at(pos);
+        ctl.tile_prefix[pos] = trun;
         trun += Tr::row_tiles ? ((ctl.pnrows[g] + kTileM - 1) / kTileM) * ntn : nmt * ntn;
       }
     }
@@ -239,13 +284,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       ctl.tile_prefix[G] = tincl;
       ctl.total_tiles = tincl;
     }
+    __syncwarp();
+    // Greedy assignment, longest first: each tile goes to the pair with the
+    // least work so far (ties to the lower pair).  Every CTA computes the same
+    // assignment and keeps its own pair's tiles; when any pair would exceed
+    // kMaxMyTiles, all pairs use the round robin instead.
+    int my_count = -1;
+    const int total_t = __shfl_sync(0xffffffffu, tincl, 31);
+    if (!Tr::row_tiles && total_t <= kMaxLptTiles && npairs <= 128) {
+      uint32_t load[4] = {0u, 0u, 0u, 0u};
+      int cnt[4] = {0, 0, 0, 0};
+      int mine = 0;
+      for (int pos = 0; pos < G; ++pos) {
+        const int g = ctl.gorder[pos];
+        const uint32_t cost = static_cast<uint32_t>(kblocks_of(g)) + 2u;  // + epilogue
+        const int base = ctl.tile_prefix[pos];
+        const int nt = ctl.tile_prefix[pos + 1] - base;
+        for (int l = 0; l < nt; ++l) {
+          uint32_t key = 0xFFFFFFFFu;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int pid = lane + 32 * q;
+            if (pid < npairs) key = min(key, (load[q] << 8) | static_cast<uint32_t>(pid));
+          }
+          key = __reduce_min_sync(0xffffffffu, key);
+          const int best = static_cast<int>(key & 0xFFu);
+          if ((best & 31) == lane) {
+            load[best >> 5] += cost;
+            ++cnt[best >> 5];
+          }
+          if (best == pair) {
+            if (lane == 0 && mine < kMaxMyTiles) ctl.my_tiles[mine] = base + l;
+            ++mine;
+          }
+        }
+      }
+      int mx = max(max(cnt[0], cnt[1]), max(cnt[2], cnt[3]));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      my_count = mx <= kMaxMyTiles ? mine : -1;
+    }
+    if (lane == 0) ctl.my_count = my_count;
   }
+  griddep_launch_dependents();
+  griddep_wait();  // the operands come from the previous kernels
   cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl.tmem_base;
   const int total = ctl.total_tiles;
   volatile int* abort_flag = &ctl.abort;
   unsigned int* dev_err = p.dev_err;
+
+  // the it-th tile of this pair (-1: none left)
+  const int my_n = ctl.my_count;
+  auto next_tile = [&](int it) -> int {
+    if (my_n >= 0) return it < my_n ? ctl.my_tiles[it] : -1;
+    const int t = pair + it * npairs;
+    return t < total ? t : -1;
+  };
 
   // k-blocks of a tile of group g
   auto tile_kblocks = [&](int g) -> int {
@@ -261,11 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t pair_tx = 2u * static_cast<uint32_t>(kStageBytes);
       int stage = 0;
       uint32_t phase = 0;
-      int g = 0, issued = 0;
+      int pos = 0, issued = 0;
       bool ok = true;
-      for (int tile = pair; tile < total && ok; tile += npairs) {
-        while (tile >= ctl.tile_prefix[g + 1]) ++g;
-        const int local = tile - ctl.tile_prefix[g];
+      for (int it = 0, tile = next_tile(0); tile >= 0 && ok; tile = next_tile(++it)) {
+        while (tile >= ctl.tile_prefix[pos + 1]) ++pos;
+        const int g = ctl.gorder[pos];
+        const int local = tile - ctl.tile_prefix[pos];
         const int m = local / ntn, n = local - m * ntn;
         const bool routed = g < p.E;
         const int nkb = tile_kblocks(g);
@@ -312,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d_pair(sb + c * 8192, mB, full_leader, ncol + c * 64, bk0 + kb * kBK, pol_b);
           }
           ++issued;
-          if (++stage == kStages) {
+          if (++stage == kSt) {
             stage = 0;
             phase ^= 1u;
           }
@@ -321,9 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok && leader) {
         int st = stage;
         uint32_t ph = phase;
-        for (int i = 0; i < kStages && i < issued; ++i) {
+        for (int i = 0; i < kSt && i < issued; ++i) {
           if (--st < 0) {
-            st = kStages - 1;
+            st = kSt - 1;
             ph ^= 1u;
           }
           volatile int local_abort = 0;
@@ -338,11 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_bf16_f32_ab(kTileM, kTileN, Tr::a_mn ? 1u : 0u, Tr::b_mn ? 1u : 0u);
       int stage = 0;
       uint32_t phase = 0;
-      int i = 0, g = 0;
+      int i = 0, pos = 0;
       bool ok = true;
-      for (int tile = pair; tile < total && ok; tile += npairs, ++i) {
-        while (tile >= ctl.tile_prefix[g + 1]) ++g;
-        const int nkb = tile_kblocks(g);
+      for (int tile = next_tile(0); tile >= 0 && ok; tile = next_tile(++i)) {
+        while (tile >= ctl.tile_prefix[pos + 1]) ++pos;
+        const int nkb = tile_kblocks(ctl.gorder[pos]);
         const int buf = i & 1;
         const uint32_t tph = (i >> 1) & 1;
         if (!mbar_wait_cluster(smem_u32(&ctl.tempty[buf]), tph ^ 1u, abort_flag, dev_err)) break;
@@ -365,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit_pair(smem_u32(&ctl.empty[stage]), 0x3);
-          if (++stage == kStages) {
+          if (++stage == kSt) {
             stage = 0;
             phase ^= 1u;
           }
@@ -385,15 +482,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r_in_tile = 128 * static_cast<int>(rank) + q * 32 + lane;
     const uint32_t tempty_leader0 = map_to_cta(smem_u32(&ctl.tempty[0]), 0);
     const uint32_t tempty_leader1 = map_to_cta(smem_u32(&ctl.tempty[1]), 0);
-    uint8_t* stage_out = smem + kStages * kStageBytes + (warp - 2) * kOutBoxBytes;
-    int g = 0, i = 0;
-    for (int tile = pair; tile < total; tile += npairs, ++i) {
-      while (tile >= ctl.tile_prefix[g + 1]) ++g;
-      const int local = tile - ctl.tile_prefix[g];
+    uint8_t* stage_out = smem + kSt * kStageBytes + (warp - 2) * out_boxes_of(kMode) * kOutBoxBytes;
+    int pos = 0, i = 0;
+    for (int tile = next_tile(0); tile >= 0; tile = next_tile(++i)) {
+      while (tile >= ctl.tile_prefix[pos + 1]) ++pos;
+      const int g = ctl.gorder[pos];
+      const int local = tile - ctl.tile_prefix[pos];
       const int m = local / ntn, n = local - m * ntn;
       const bool routed = g < p.E;
       const int buf = i & 1;
       const uint32_t tph = (i >> 1) & 1;
+      // the activation mode's h_bar rows do not depend on this kernel: load
+      // them before waiting for the accumulator
+      uint32_t hbp[2][16];
+      if (kMode == kActBwd) {
+        const int row = m * kTileM + r_in_tile;
+        if (row < ctl.pnrows[g]) {
+          const size_t orow = static_cast<size_t>(ctl.prow0[g] + row);
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const int col = n * hw + part * (hw / 2) + 32 * c2;
+            if (col < p.N) load_bf16x32(p.hbar + orow * p.N + col, hbp[c2]);
+          }
+        }
+      }
       const bool got = mbar_wait_cluster(smem_u32(&ctl.tfull[buf]), tph, abort_flag, dev_err);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
@@ -407,44 +519,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int warp_row0 = m * kTileM + 128 * static_cast<int>(rank) + q * 32;
         const bool full_box = warp_row0 + kOutBoxRows <= nvalid;
         const int col0 = n * hw;
-        for (int cc = part * cols_per_part; cc < (part + 1) * cols_per_part; cc += kOutBoxCols) {
+        constexpr int kChunks = (kMode == kActBwd ? kTileN / 2 : kTileN) / 2 / kOutBoxCols;
+#pragma unroll
+        for (int c2 = 0; c2 < kChunks; ++c2) {
+          const int cc = part * cols_per_part + c2 * kOutBoxCols;
           if (col0 + cc >= p.N) break;
           if (kMode == kActBwd) {
             uint32_t rg[32], ru[32];
             tmem_ld_32cols(taddr + cc, rg);
             tmem_ld_32cols(taddr + hw + cc, ru);
             tmem_ld_wait();
-            if (!valid) continue;
-            const size_t orow = static_cast<size_t>(orow0 + row);
-            uint32_t hb[16];
-            load_bf16x32(p.hbar + orow * p.N + col0 + cc, hb);
-            uint32_t og[16], ou[16], oh[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              float gg[2], uu[2], hh[2], gb[2], ub[2], hv[2];
-              gg[0] = __uint_as_float(rg[2 * j]);
-              gg[1] = __uint_as_float(rg[2 * j + 1]);
-              uu[0] = __uint_as_float(ru[2 * j]);
-              uu[1] = __uint_as_float(ru[2 * j + 1]);
-              hh[0] = bf16_lo(hb[j]);
-              hh[1] = bf16_hi(hb[j]);
-#pragma unroll
-              for (int t = 0; t < 2; ++t) {
-                const float e = __expf(-gg[t]);
-                const float sig = __fdividef(1.0f, 1.0f + e);
-                const float silu = __fdividef(gg[t], 1.0f + e);  // the forward's expression
-                hv[t] = silu * uu[t];
-                // silu'(g) = sigmoid(g) (1 + g (1 - sigmoid(g)))
-                gb[t] = hh[t] * uu[t] * (sig * (1.0f + gg[t] * (1.0f - sig)));
-                ub[t] = hh[t] * silu;
-              }
-              og[j] = pack_bf16x2(gb[0], gb[1]);
-              ou[j] = pack_bf16x2(ub[0], ub[1]);
-              oh[j] = pack_bf16x2(hv[0], hv[1]);
+            const uint32_t(&hb)[16] = hbp[c2 < 2 ? c2 : 1];
+            if (full_box) {
+              bulk_wait_group_read0();  // the previous chunk's stores have read the buffers
+              __syncwarp();
             }
-            store_bf16x32(p.gu + orow * (2 * p.N) + col0 + cc, og);
-            store_bf16x32(p.gu + orow * (2 * p.N) + p.N + col0 + cc, ou);
-            store_bf16x32(p.h + orow * p.N + col0 + cc, oh);
+            const size_t orow = static_cast<size_t>(orow0 + (valid ? row : 0));
+            // 16-byte chunk v of the row: columns 8 v .. 8 v + 7 of the box
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t og[4], ou[4], oh[4];
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {
+                const int j = 4 * v + jj;
+                float gb[2], ub[2], hv[2];
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                  const float gg = __uint_as_float(rg[2 * j + t]);
+                  const float uu = __uint_as_float(ru[2 * j + t]);
+                  const float hh = t ? bf16_hi(hb[j]) : bf16_lo(hb[j]);
+                  const float e = __expf(-gg);
+                  const float sig = __fdividef(1.0f, 1.0f + e);
+                  const float silu = __fdividef(gg, 1.0f + e);  // the forward's expression
+                  hv[t] = silu * uu;
+                  // silu'(g) = sigmoid(g) (1 + g (1 - sigmoid(g)))
+                  gb[t] = hh * uu * (sig * (1.0f + gg * (1.0f - sig)));
+                  ub[t] = hh * silu;
+                }
+                og[jj] = pack_bf16x2(gb[0], gb[1]);
+                ou[jj] = pack_bf16x2(ub[0], ub[1]);
+                oh[jj] = pack_bf16x2(hv[0], hv[1]);
+              }
+              if (full_box) {
+                const int sw = lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4);
+                *reinterpret_cast<uint4*>(stage_out + sw) = make_uint4(og[0], og[1], og[2], og[3]);
+                *reinterpret_cast<uint4*>(stage_out + kOutBoxBytes + sw) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+                *reinterpret_cast<uint4*>(stage_out + 2 * kOutBoxBytes + sw) =
+                    make_uint4(oh[0], oh[1], oh[2], oh[3]);
+              } else if (valid) {
+                uint16_t* gdst = p.gu + orow * (2 * p.N) + col0 + cc + 8 * v;
+                *reinterpret_cast<uint4*>(gdst) = make_uint4(og[0], og[1], og[2], og[3]);
+                *reinterpret_cast<uint4*>(gdst + p.N) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+                *reinterpret_cast<uint4*>(p.h + orow * p.N + col0 + cc + 8 * v) =
+                    make_uint4(oh[0], oh[1], oh[2], oh[3]);
+              }
+            }
+            if (full_box) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                const int r0 = orow0 + warp_row0;
+                tma_store_2d(&mapC, smem_u32(stage_out), col0 + cc, r0);
+                tma_store_2d(&mapC, smem_u32(stage_out + kOutBoxBytes), p.N + col0 + cc, r0);
+                tma_store_2d(&mapC2, smem_u32(stage_out + 2 * kOutBoxBytes), col0 + cc, r0);
+                bulk_commit_group();
+              }
+            }
           } else {
             uint32_t ra[32];
             tmem_ld_32cols(taddr + cc, ra);
@@ -529,12 +669,12 @@ std::mutex g_bwd_mu;
 template <int kMode>
 cudaError_t mode_setup(int sms, int* pairs) {
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_bwd_kernel<kMode>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_of(kMode));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes_of(kMode);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -569,7 +709,7 @@ cudaError_t bwd_setup(BwdDevice* out) {
 }
 
 template <int kMode>
-cudaError_t launch_mode(const CUtensorMap (&m)[7], BwdArgs a, cudaStream_t s, bool pdl) {
+cudaError_t launch_mode(const CUtensorMap (&m)[8], BwdArgs a, cudaStream_t s, bool pdl) {
   BwdDevice bd;
   cudaError_t e = bwd_setup(&bd);
   if (e != cudaSuccess) return e;
@@ -577,7 +717,7 @@ cudaError_t launch_mode(const CUtensorMap (&m)[7], BwdArgs a, cudaStream_t s, bo
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * bd.pairs[kMode], 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes_of(kMode);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -588,7 +728,8 @@ cudaError_t launch_mode(const CUtensorMap (&m)[7], BwdArgs a, cudaStream_t s, bo
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  e = cudaLaunchKernelEx(&cfg, grouped_gemm_bwd_kernel<kMode>, m[0], m[1], m[2], m[3], m[4], m[5], m[6], a);
+  e = cudaLaunchKernelEx(&cfg, grouped_gemm_bwd_kernel<kMode>, m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7],
+                         a);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -612,7 +753,7 @@ cudaError_t launch_bwd_dgrad_w2(const BwdLayout& L, const int32_t* offsets, cons
                                 uint16_t* hbar, cudaStream_t s, bool pdl) {
   const moe_dims& d = L.d;
   const uint64_t rows = static_cast<uint64_t>(L.S_pad) + (L.shared ? d.T : 0);
-  CUtensorMap m[7];
+  CUtensorMap m[8];
   cudaError_t e;
   if ((e = tensor_map_2d(&m[0], ybar, L.S_pad, d.D, 128, kBK)) != cudaSuccess) return e;
   if ((e = tensor_map_2d(&m[2], W2, static_cast<uint64_t>(d.E) * d.F, d.D, 128, kBK)) != cudaSuccess) return e;
@@ -631,6 +772,7 @@ cudaError_t launch_bwd_dgrad_w2(const BwdLayout& L, const int32_t* offsets, cons
   a.N = d.F;
   a.b_rows = d.F;
   a.C = hbar;
+  m[7] = m[6];
   return launch_mode<kDgradW2>(m, a, s, pdl);
 }
 
@@ -640,7 +782,7 @@ cudaError_t launch_bwd_act(const BwdLayout& L, const int32_t* offsets, const uin
                            uint16_t* gu, uint16_t* h, cudaStream_t s, bool pdl) {
   const moe_dims& d = L.d;
   const int S = d.T * d.k;
-  CUtensorMap m[7];
+  CUtensorMap m[8];
   cudaError_t e;
   if ((e = tensor_map_2d(&m[0], x_sorted, S, d.D, 128, kBK)) != cudaSuccess) return e;
   if ((e = tensor_map_2d(&m[2], W1, static_cast<uint64_t>(d.E) * d.D, d.F, kBK, 64)) != cudaSuccess) return e;
@@ -654,7 +796,9 @@ cudaError_t launch_bwd_act(const BwdLayout& L, const int32_t* offsets, const uin
     m[4] = m[2];
     m[5] = m[3];
   }
-  m[6] = m[0];  // no TMA store in this mode
+  const uint64_t rows = static_cast<uint64_t>(L.S_pad) + (L.shared ? d.T : 0);
+  if ((e = tensor_map_2d(&m[6], gu, rows, 2 * d.F, kOutBoxRows, kOutBoxCols)) != cudaSuccess) return e;
+  if ((e = tensor_map_2d(&m[7], h, rows, d.F, kOutBoxRows, kOutBoxCols)) != cudaSuccess) return e;
   BwdArgs a = base_args(L, offsets);
   a.K = d.D;
   a.N = d.F;
@@ -669,7 +813,7 @@ cudaError_t launch_bwd_dgrad_x(const BwdLayout& L, const int32_t* offsets, const
                                const uint16_t* Ws3, uint16_t* xbar, cudaStream_t s, bool pdl) {
   const moe_dims& d = L.d;
   const uint64_t rows = static_cast<uint64_t>(L.S_pad) + (L.shared ? d.T : 0);
-  CUtensorMap m[7];
+  CUtensorMap m[8];
   cudaError_t e;
   if ((e = tensor_map_2d(&m[0], gu, L.S_pad, 2 * d.F, 128, kBK)) != cudaSuccess) return e;
   if ((e = tensor_map_2d(&m[2], W1, static_cast<uint64_t>(d.E) * d.D, d.F, 128, kBK)) != cudaSuccess) return e;
@@ -691,6 +835,7 @@ cudaError_t launch_bwd_dgrad_x(const BwdLayout& L, const int32_t* offsets, const
   a.N = d.D;
   a.b_rows = d.D;
   a.C = xbar;
+  m[7] = m[6];
   return launch_mode<kDgradX>(m, a, s, pdl);
 }
 
@@ -700,7 +845,7 @@ cudaError_t launch_bwd_wgrad(const BwdLayout& L, const int32_t* offsets, const u
                              float* ws_b, cudaStream_t s, bool pdl) {
   const moe_dims& d = L.d;
   const int S = d.T * d.k;
-  CUtensorMap m[7];
+  CUtensorMap m[8];
   cudaError_t e;
   if ((e = tensor_map_2d(&m[0], A, a_padded ? L.S_pad : S, M, kBK, 64)) != cudaSuccess) return e;
   if ((e = tensor_map_2d(&m[2], B, L.S_pad, N, kBK, 64)) != cudaSuccess) return e;
@@ -723,6 +868,7 @@ cudaError_t launch_bwd_wgrad(const BwdLayout& L, const int32_t* offsets, const u
   a.w_b = w_b;
   a.ws_a = ws_a;
   a.ws_b = ws_b;
+  m[7] = m[6];
   return launch_mode<kWgrad>(m, a, s, pdl);
 }
 

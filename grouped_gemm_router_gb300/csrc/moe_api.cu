@@ -72,6 +72,7 @@ struct BwdWorkspace {
   float* wbar;     // [T, k]
   float* lbar;     // [T, k]
   float* rpart;    // router-gradient partials
+  uint16_t* wgt;   // Wg^T [E, D]
   size_t bytes;
 };
 
@@ -94,6 +95,7 @@ BwdWorkspace carve_bwd(void* base, const moe_dims& d, bool shared) {
   w.wbar = reinterpret_cast<float*>(take(S * 4));
   w.lbar = reinterpret_cast<float*>(take(S * 4));
   w.rpart = reinterpret_cast<float*>(take(bwd_router_part_floats(d) * 4));
+  w.wgt = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(d.E) * d.D * 2));
   w.bytes = off;
   return w;
 }
@@ -201,7 +203,7 @@ moe_status run_backward(const uint16_t* x, const uint16_t* Wg, const uint16_t* W
   cudaError_t e;
   record(o, 0, s);
   e = launch_combine_bwd(L, d_out, fw.y, w, ids, fw.inv, fw.offsets, routed_in ? 1 : 0, bw.ybar, bw.wbar,
-                         bw.lbar, s, false);
+                         bw.lbar, Wg, bw.wgt, s, false);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(o, 1, s);
   e = launch_bwd_dgrad_w2(L, fw.offsets, bw.ybar, d_out, W2, Ws2, bw.hbar, s, true);
@@ -216,19 +218,20 @@ moe_status run_backward(const uint16_t* x, const uint16_t* Wg, const uint16_t* W
   e = launch_bwd_wgrad(L, fw.offsets, fw.x_sorted, 0, d.D, x, bw.gu, 2 * d.F, bw.gu + Sp * 2 * d.F, d.F,
                        dW1, dW3, dWs1, dWs3, s, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
+  record(o, 5, s);
   e = launch_bwd_wgrad(L, fw.offsets, bw.h, 1, d.F, bw.h + Sp * d.F, bw.ybar, d.D, d_out, d.D, dW2,
                        nullptr, dWs2, nullptr, s, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  record(o, 5, s);
-  e = launch_dx_gather(L, bw.xbar, ids, fw.inv, fw.offsets, routed_in ? nullptr : bw.lbar, Wg, dx, s,
-                       true);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(o, 6, s);
+  e = launch_dx_gather(L, bw.xbar, ids, fw.inv, fw.offsets, routed_in ? nullptr : bw.lbar, bw.wgt, dx,
+                       s, true);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  record(o, 7, s);
   if (!routed_in && (dWg != nullptr || dbias != nullptr)) {
-    e = launch_router_bwd(L, x, ids, bw.lbar, bw.rpart, dWg, dbias, s, true);
+    e = launch_router_bwd(L, fw.x_sorted, fw.perm, fw.offsets, bw.lbar, bw.rpart, dWg, dbias, s, true);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
-  record(o, 7, s);
+  record(o, 8, s);
   return MOE_OK;
 }
 

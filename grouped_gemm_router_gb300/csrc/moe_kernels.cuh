@@ -104,20 +104,22 @@ cudaError_t launch_bwd_wgrad(const BwdLayout& L, const int32_t* offsets, const u
                              float* ws_b, cudaStream_t s, bool pdl);
 // Combine backward: y_bar (padded layout, padding rows zeroed), the gradient of
 // the gate weights and of the selected logits (zero when routed_in).
+// Also writes Wg^T [E, D] into wgt (unless routed_in).
 cudaError_t launch_combine_bwd(const BwdLayout& L, const uint16_t* d_out, const uint16_t* y,
                                const float* w, const int32_t* ids, const int32_t* inv,
                                const int32_t* offsets, int routed_in, uint16_t* ybar, float* wbar,
-                               float* lbar, cudaStream_t s, bool pdl);
-// dx[t] = sum_j x_bar[slot j] (+ x_bar[shared row]) + sum_j lbar[t,j] Wg[:, ids[t,j]].
+                               float* lbar, const uint16_t* Wg, uint16_t* wgt, cudaStream_t s, bool pdl);
+// dx[t] = sum_j x_bar[slot j] (+ x_bar[shared row]) + sum_j lbar[t,j] Wg^T[ids[t,j], :].
 cudaError_t launch_dx_gather(const BwdLayout& L, const uint16_t* xbar, const int32_t* ids,
                              const int32_t* inv, const int32_t* offsets, const float* lbar,
-                             const uint16_t* Wg, uint16_t* dx, cudaStream_t s, bool pdl);
-// dWg = x^T logits_bar and dbias = column sums of logits_bar, via per-chunk
-// partials (deterministic); `part` holds bwd_router_part_floats(d) floats.
+                             const uint16_t* wgt, uint16_t* dx, cudaStream_t s, bool pdl);
+// dWg[:, e] = sum over expert e's sorted rows of l_bar[perm[p]] x_sorted[p] and
+// dbias[e] = sum of those l_bar, via group-aligned chunk partials summed in
+// order (deterministic); `part` holds bwd_router_part_floats(d) floats.
 size_t bwd_router_part_floats(const moe_dims& d);
-cudaError_t launch_router_bwd(const BwdLayout& L, const uint16_t* x, const int32_t* ids,
-                              const float* lbar, float* part, float* dWg, float* dbias,
-                              cudaStream_t s, bool pdl);
+cudaError_t launch_router_bwd(const BwdLayout& L, const uint16_t* x_sorted, const int32_t* perm,
+                              const int32_t* offsets, const float* lbar, float* part, float* dWg,
+                              float* dbias, cudaStream_t s, bool pdl);
 
 // 2-D bf16 TMA descriptor of a row-major [rows, cols] matrix with a
 // {box_cols, box_rows} box: 128-byte swizzle (64-byte for 32-column boxes),

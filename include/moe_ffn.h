@@ -74,8 +74,9 @@ typedef struct {
    * [0] before routing, [1] after routing, [2] after the permutation,
    * [3] after W1||W3, [4] after W2, [5] after the combine.
    * moe_ffn_forward_host records [6] after the host->device copy of x (before
-   * [0]) and [7] after the device->host copy of out.  NULL entries are skipped. */
-  void* stage_events[8];
+   * [0]) and [7] after the device->host copy of out.  moe_ffn_backward uses
+   * [0..8] (see there).  NULL entries are skipped. */
+  void* stage_events[12];
   /* Routing fixed from outside: ids [T, k] int32 and weights [T, k] fp32 in
    * device memory replace the router when both are non-NULL. */
   const int32_t* ids_in;
@@ -134,9 +135,9 @@ moe_status moe_ffn_forward_host(const void* x_host, const void* Wg, const float*
  * 256-byte aligned: y_bar [S_pad, D], h_bar [R, F], g_bar|u_bar [R, 2F],
  * h [R, F], x_bar [R, D] (bf16, the routed rows of each expert padded to a
  * multiple of 64 rows in expert order, the shared rows from S_pad), the
- * gate-weight and selected-logit gradients [T, k] fp32 and the router-
- * gradient partials (ceil(T/256) * (D*E + E) fp32).  0 for unsupported
- * dimensions. */
+ * gate-weight and selected-logit gradients [T, k] fp32, the router-
+ * gradient partials ((T*k/256 + E) * (D + 1) fp32) and Wg^T [E, D] bf16.
+ * 0 for unsupported dimensions. */
 size_t moe_ffn_backward_workspace_size(moe_dims d, int has_shared);
 
 /* Gradients of L = sum(d_out * out) for the layer moe_ffn_forward computed
@@ -158,9 +159,9 @@ size_t moe_ffn_backward_workspace_size(moe_dims d, int has_shared);
  *   gradient.
  *   opts (nullable): ids_in / weights_in must repeat the fixed routing the
  *   forward was given, and then the router gets no gradient (dWg, dbias and
- *   the router term of dx are zero / skipped); stage_events [0..7] are
+ *   the router term of dx are zero / skipped); stage_events [0..8] are
  *   recorded before the combine backward, after it, after h_bar, after
- *   g_bar|u_bar, after x_bar, after the weight gradients, after dx and after
+ *   g_bar|u_bar, after x_bar, after dW1|dW3, after dW2, after dx and after
  *   the router gradient; flags must be 0.
  *   Precision: fp32 accumulation everywhere; y_bar, h_bar, g_bar, u_bar, h
  *   and x_bar are stored as bf16 between the GEMMs; dx is summed in fp32 and

@@ -133,7 +133,7 @@ def test_backward_workspace_size_matches_documented_layout(native):
         Sp = S + 64 * E
         R = Sp + (T if sh else 0)
         n = a(Sp * D * 2) + a(R * F * 2) + a(R * F * 4) + a(R * F * 2) + a(R * D * 2) + 2 * a(S * 4)
-        n += a(((T + 255) // 256) * (D * E + E) * 4)
+        n += a((S // 256 + E) * (D + 1) * 4) + a(E * D * 2)
         assert native.lib.moe_ffn_backward_workspace_size(native.dims(T, D, F, E, k), sh) == n
 
 
