@@ -174,3 +174,43 @@ def test_concurrent_calls_from_host_threads(moe):
     for o in outs:
         assert torch.equal(o, ref)
     assert moe.device_error() == 0
+
+
+def test_forward_and_backward_replay_from_a_cuda_graph(moe):
+    """The launch sequences capture into a CUDA graph (kernels on the caller's
+    stream, programmatic dependent launch edges kept) and replay to the eager
+    results bit for bit."""
+    w_, L = inputs.make_custom(1500, 256, 512, 8, 2, True, 61)
+    G = _dev_layer(L)
+    T, D, F, E, k = w_.T, w_.D, w_.F, w_.E, w_.k
+    rng = np.random.default_rng(2)
+    d_out = to_dev(inputs.f32_to_bf16_bits(rng.standard_normal((T, D)).astype(np.float32)))
+    ws = moe.Workspace(T, D, F, E, k, True)
+    bws = moe.BackwardWorkspace(T, D, F, E, k, True)
+    out = torch.empty(T, D, dtype=torch.bfloat16, device="cuda")
+    sh = dict(Ws1=G["Ws1"], Ws3=G["Ws3"], Ws2=G["Ws2"])
+
+    def step():
+        moe.moe_ffn_forward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], k, out=out, workspace=ws, **sh)
+        return moe.moe_ffn_backward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], k, d_out, ws,
+                                    bwd_workspace=bws, **sh)
+
+    eager_g = step()
+    torch.cuda.synchronize()
+    eager_out = out.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()                       # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        graph_g = step()
+    out.zero_()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert moe.device_error() == 0
+    assert torch.equal(out, eager_out)
+    for name in eager_g:
+        assert torch.equal(graph_g[name], eager_g[name]), name
