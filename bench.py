@@ -39,6 +39,7 @@ if ROOT not in sys.path:
 from grouped_gemm_router_gb300 import inputs  # noqa: E402
 
 WORKLOAD = "gptoss_lite"
+DATASHEET_BF16_DENSE_TFLOPS = 2250.0  # GB300 dense bf16 (the datasheet's sparse figure halved)
 METRIC = "MoE FFN fwd tokens/s and active TFLOP/s on 1 GB300; % of bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -631,8 +632,10 @@ def main():
         "config": {"workload": w.name, "T": w.T, "D": w.D, "F": w.F, "E": w.E, "k": w.k,
                    "shared_expert": w.shared, "l2": "flushed between steps (512 MB write + read back)",
                    "parallelism": f"replicas x{world}"},
+        "ms_per_step_median": float(np.median(step_ms)),
         "active_tflops": fl * world / (ms / 1e3) / 1e12,
         "frac_of_bf16_peak": fl / (ms / 1e3) / 1e12 / pk["bf16_tflops"],
+        "frac_of_datasheet_bf16_dense": fl / (ms / 1e3) / 1e12 / DATASHEET_BF16_DENSE_TFLOPS,
         "stage_ms": st_mean,
         "stage_ms_note": f"{KB} extra steps with an event at every stage boundary (serialised launches)",
         "roofline": {"bound": "tensor", "kernel": "grouped_gemm_pair_kernel<true> (W1||W3 + SiLU*mul)",

@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(256) pack_router_weights_kernel(const uint16_t
 
 // Resident blocks per SM the register budget is sized for: all blocks of a
 // 32K-token batch (512 blocks) fit in one wave for E <= 8.
-constexpr int route_min_blocks(int nt) { return nt <= 1 ? 3 : nt <= 2 ? 3 : nt <= 8 ? 2 : 1; }
+constexpr int route_min_blocks(int nt) { return nt <= 1 ? 4 : nt <= 2 ? 3 : nt <= 8 ? 2 : 1; }
 
 // Block = 8 warps for TB = 16 MT tokens (MT = 1, 2 or 4 tiles of 16 tokens).
 // Warp w computes tile w % MT over the 32-wide D-chunks kc with
@@ -96,8 +96,6 @@ __global__ void __launch_bounds__(kRouteThreads, route_min_blocks(NT)) route_ker
   extern __shared__ float red[];  // [8 warps][NT][4][32]: partial logits
   __shared__ int s_hist[MOE_MAX_EXPERTS];
 
-  griddep_wait();  // packed weights (and, in a layer, nothing else) come from the previous kernel
-  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int MT = TB >> 4, DS = 8 / MT;
@@ -116,9 +114,8 @@ __global__ void __launch_bounds__(kRouteThreads, route_min_blocks(NT)) route_ker
 
   constexpr int KG = (NT >= 16) ? 1 : (NT >= 8) ? 2 : 4;  // chunks per load batch
   const int nkc = D >> 5;
-  for (int kc0 = split; kc0 < nkc; kc0 += KG * DS) {
-    // all loads of the batch first: x (2 rows x KG chunks) and the weights
-    uint4 a0[KG], a1[KG], b[KG][NT];
+  uint4 a0[KG], a1[KG];
+  auto load_x = [&](int kc0) {  // x of one batch: 2 rows x KG chunks
 #pragma unroll
     for (int j = 0; j < KG; ++j) {
       const int kc = kc0 + j * DS;
@@ -126,6 +123,20 @@ __global__ void __launch_bounds__(kRouteThreads, route_min_blocks(NT)) route_ker
       const int q = (kc << 2) + c;  // 16-byte column index
       a0[j] = (ok0 && in) ? __ldg(xr0 + q) : make_uint4(0, 0, 0, 0);
       a1[j] = (ok1 && in) ? __ldg(xr1 + q) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  // x does not come from the previous kernel (the weight packing): start
+  // streaming it before waiting for the packed weights
+  load_x(split);
+  griddep_wait();
+  griddep_launch_dependents();
+  for (int kc0 = split; kc0 < nkc; kc0 += KG * DS) {
+    if (kc0 != split) load_x(kc0);
+    uint4 b[KG][NT];
+#pragma unroll
+    for (int j = 0; j < KG; ++j) {
+      const int kc = kc0 + j * DS;
+      const bool in = kc < nkc;
 #pragma unroll
       for (int n = 0; n < NT; ++n)
         b[j][n] = in ? __ldg(wpack + (static_cast<size_t>(kc) * NT + n) * 32 + lane) : make_uint4(0, 0, 0, 0);
