@@ -62,6 +62,9 @@ enum : int { kDgradW2 = 0, kActBwd = 1, kDgradX = 2, kWgrad = 3 };
 // of them are assigned longest first to the least-loaded pair.
 constexpr int kMaxLptTiles = 2048;
 constexpr int kMaxMyTiles = 64;
+// A weight-gradient group longer than kMaxChunkKb k-blocks is split along K
+// into near-equal chunks whose fp32 partial sums a reduction kernel adds.
+constexpr int kMaxChunkKb = 160;
 
 // The activation mode stages three output boxes per epilogue warp (g_bar,
 // u_bar, h) and gives up one stage of the ring for them.
@@ -94,13 +97,14 @@ struct BwdArgs {
   // kActBwd
   const uint16_t* hbar;    // [S_pad + T, N] incoming gradient of h
   uint16_t* gu;            // [S_pad + T, 2N] g_bar | u_bar
-  uint16_t* h;             // [S_pad + T, N] recomputed h
+  uint16_t* h;             // [S_pad + T, N] recomputed h, or NULL: not stored
   // kWgrad: fp32 outputs; columns [0, n_split) go to *_a, [n_split, N) to *_b
   float* w_a;
   float* w_b;
   float* ws_a;
   float* ws_b;
   int n_split;
+  float* part;             // kWgrad: partial sums of split groups [slot][M][N]
   unsigned int* dev_err;
 };
 
@@ -121,6 +125,8 @@ struct BwdCtl {
   int prow0[kMaxGroups];  // padded first row (shared group: S_pad)
   int nrows[kMaxGroups];
   int pnrows[kMaxGroups];
+  int nchunk[kMaxGroups];  // kWgrad: K chunks of the group
+  int pslot[kMaxGroups];   // kWgrad: first partial slot of a split group
 };
 
 // Reads one bf16 x 32 chunk (64 bytes) into 16 packed words.
@@ -171,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntn = (p.N + hw - 1) / hw;
   const int nmt = (p.M + kTileM - 1) / kTileM;  // kWgrad
   const int half_n = kTileN / 2;
+  const bool want_h = kMode == kActBwd && p.h != nullptr;  // kActBwd: also store the recomputed h
 
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&mapA);
@@ -236,14 +243,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     // weight gradients: groups by decreasing length (ties by index), so the
     // greedy assignment below sees the longest tiles first
     auto kblocks_of = [&](int g) { return (ctl.pnrows[g] + kBK - 1) / kBK; };
+    auto nchunk_of = [&](int g) { return max(1, (kblocks_of(g) + kMaxChunkKb - 1) / kMaxChunkKb); };
+    auto chunk_kb_of = [&](int g) { return (kblocks_of(g) + nchunk_of(g) - 1) / nchunk_of(g); };
     if (!Tr::row_tiles) {
+      // partial slots of the split groups, in group order
+      int nsl = 0;
       for (int i = 0; i < per; ++i) {
         const int g = lane * per + i;
         if (g < G) {
-          const int c = kblocks_of(g);
+          ctl.nchunk[g] = nchunk_of(g);
+          nsl += ctl.nchunk[g] > 1 ? ctl.nchunk[g] : 0;
+        }
+      }
+      int sincl = nsl;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, sincl, off);
+        if (lane >= off) sincl += v;
+      }
+      int srun = sincl - nsl;
+      for (int i = 0; i < per; ++i) {
+        const int g = lane * per + i;
+        if (g < G) {
+          ctl.pslot[g] = srun;
+          srun += ctl.nchunk[g] > 1 ? ctl.nchunk[g] : 0;
+        }
+      }
+      for (int i = 0; i < per; ++i) {
+        const int g = lane * per + i;
+        if (g < G) {
+          const int c = chunk_kb_of(g);
           int rnk = 0;
           for (int h = 0; h < G; ++h) {
-            const int ch = kblocks_of(h);
+            const int ch = chunk_kb_of(h);
             rnk += (ch > c || (ch == c && h < g)) ? 1 : 0;
           }
           ctl.gorder[rnk] = g;
@@ -262,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pos = lane * per + i;
       if (pos < G) {
         const int g = group_at(pos);
-        tl += Tr::row_tiles ? ((ctl.pnrows[g] + kTileM - 1) / kTileM) * ntn : nmt * ntn;
+        tl += Tr::row_tiles ? ((ctl.pnrows[g] + kTileM - 1) / kTileM) * ntn : nchunk_of(g) * nmt * ntn;
       }
     }
     int tincl = tl;
@@ -277,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pos < G) {
         const int g = group_at(pos);
         ctl.tile_prefix[pos] = trun;
-        trun += Tr::row_tiles ? ((ctl.pnrows[g] + kTileM - 1) / kTileM) * ntn : nmt * ntn;
+        trun += Tr::row_tiles ? ((ctl.pnrows[g] + kTileM - 1) / kTileM) * ntn : nchunk_of(g) * nmt * ntn;
       }
     }
     if (lane == 31) {
@@ -297,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int mine = 0;
       for (int pos = 0; pos < G; ++pos) {
         const int g = ctl.gorder[pos];
-        const uint32_t cost = static_cast<uint32_t>(kblocks_of(g)) + 2u;  // + epilogue
+        const uint32_t cost = static_cast<uint32_t>(chunk_kb_of(g)) + 2u;  // + epilogue
         const int base = ctl.tile_prefix[pos];
         const int nt = ctl.tile_prefix[pos + 1] - base;
         for (int l = 0; l < nt; ++l) {
@@ -343,10 +375,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     return t < total ? t : -1;
   };
 
-  // k-blocks of a tile of group g
-  auto tile_kblocks = [&](int g) -> int {
-    if (Tr::row_tiles) return p.K / kBK;
-    return (ctl.pnrows[g] + kBK - 1) / kBK;
+  // Coordinates of a tile (its local index within group g): K chunk c, m and n
+  // tiles, and its k-block range [kb0, kb1).  Weight-gradient tiles are
+  // numbered chunk by chunk, so the tiles reading the same rows run together.
+  struct TileInfo {
+    int c, m, n, kb0, kb1;
+  };
+  auto tile_info = [&](int g, int local) -> TileInfo {
+    TileInfo t;
+    if (Tr::row_tiles) {
+      t.c = 0;
+      t.m = local / ntn;
+      t.n = local - t.m * ntn;
+      t.kb0 = 0;
+      t.kb1 = p.K / kBK;
+    } else {
+      const int per_chunk = nmt * ntn;
+      t.c = local / per_chunk;
+      const int r = local - t.c * per_chunk;
+      t.m = r / ntn;
+      t.n = r - t.m * ntn;
+      const int nkb = (ctl.pnrows[g] + kBK - 1) / kBK;
+      const int csz = (nkb + ctl.nchunk[g] - 1) / ctl.nchunk[g];
+      t.kb0 = t.c * csz;
+      t.kb1 = min(t.kb0 + csz, nkb);
+    }
+    return t;
   };
 
   if (warp == 0) {
@@ -363,11 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (tile >= ctl.tile_prefix[pos + 1]) ++pos;
         const int g = ctl.gorder[pos];
         const int local = tile - ctl.tile_prefix[pos];
-        const int m = local / ntn, n = local - m * ntn;
+        const TileInfo ti = tile_info(g, local);
+        const int m = ti.m, n = ti.n;
         const bool routed = g < p.E;
-        const int nkb = tile_kblocks(g);
         const CUtensorMap* mA = routed ? &mapA : &mapA_sh;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
           if (!mbar_wait_cluster(smem_u32(&ctl.empty[stage]), phase ^ 1u, abort_flag, dev_err)) {
             ok = false;
             break;
@@ -439,13 +493,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = next_tile(0); tile >= 0 && ok; tile = next_tile(++i)) {
         while (tile >= ctl.tile_prefix[pos + 1]) ++pos;
-        const int nkb = tile_kblocks(ctl.gorder[pos]);
+        const TileInfo ti = tile_info(ctl.gorder[pos], tile - ctl.tile_prefix[pos]);
         const int buf = i & 1;
         const uint32_t tph = (i >> 1) & 1;
         if (!mbar_wait_cluster(smem_u32(&ctl.tempty[buf]), tph ^ 1u, abort_flag, dev_err)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + buf * 256;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
           if (!mbar_wait_cluster(smem_u32(&ctl.full[stage]), phase, abort_flag, dev_err)) {
             ok = false;
             break;
@@ -459,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             : smem_desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bdesc = Tr::b_mn ? smem_desc_sw128(sb + kk * 2048, 8192, 1024)
                                             : smem_desc_sw128(sb + kk * 32, 16, 1024);
-            umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb != ti.kb0 || kk != 0) ? 1u : 0u);
           }
           umma_commit_pair(smem_u32(&ctl.empty[stage]), 0x3);
           if (++stage == kSt) {
@@ -488,7 +542,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (tile >= ctl.tile_prefix[pos + 1]) ++pos;
       const int g = ctl.gorder[pos];
       const int local = tile - ctl.tile_prefix[pos];
-      const int m = local / ntn, n = local - m * ntn;
+      const TileInfo ti = tile_info(g, local);
+      const int m = ti.m, n = ti.n;
       const bool routed = g < p.E;
       const int buf = i & 1;
       const uint32_t tph = (i >> 1) & 1;
@@ -564,14 +619,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int sw = lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4);
                 *reinterpret_cast<uint4*>(stage_out + sw) = make_uint4(og[0], og[1], og[2], og[3]);
                 *reinterpret_cast<uint4*>(stage_out + kOutBoxBytes + sw) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
-                *reinterpret_cast<uint4*>(stage_out + 2 * kOutBoxBytes + sw) =
-                    make_uint4(oh[0], oh[1], oh[2], oh[3]);
+                if (want_h)
+                  *reinterpret_cast<uint4*>(stage_out + 2 * kOutBoxBytes + sw) =
+                      make_uint4(oh[0], oh[1], oh[2], oh[3]);
               } else if (valid) {
                 uint16_t* gdst = p.gu + orow * (2 * p.N) + col0 + cc + 8 * v;
                 *reinterpret_cast<uint4*>(gdst) = make_uint4(og[0], og[1], og[2], og[3]);
                 *reinterpret_cast<uint4*>(gdst + p.N) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
-                *reinterpret_cast<uint4*>(p.h + orow * p.N + col0 + cc + 8 * v) =
-                    make_uint4(oh[0], oh[1], oh[2], oh[3]);
+                if (want_h)
+                  *reinterpret_cast<uint4*>(p.h + orow * p.N + col0 + cc + 8 * v) =
+                      make_uint4(oh[0], oh[1], oh[2], oh[3]);
               }
             }
             if (full_box) {
@@ -581,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int r0 = orow0 + warp_row0;
                 tma_store_2d(&mapC, smem_u32(stage_out), col0 + cc, r0);
                 tma_store_2d(&mapC, smem_u32(stage_out + kOutBoxBytes), p.N + col0 + cc, r0);
-                tma_store_2d(&mapC2, smem_u32(stage_out + 2 * kOutBoxBytes), col0 + cc, r0);
+                if (want_h) tma_store_2d(&mapC2, smem_u32(stage_out + 2 * kOutBoxBytes), col0 + cc, r0);
                 bulk_commit_group();
               }
             }
@@ -613,8 +670,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        // kWgrad: fp32 rows m * 256 + r (< M), columns n * 256 + cc (< N)
-        const int nkb = tile_kblocks(g);
+        // kWgrad: fp32 rows m * 256 + r (< M), columns n * 256 + cc (< N);
+        // a split group's chunk goes to its partial slot
+        const bool empty_k = ti.kb1 <= ti.kb0;
+        const bool split = ctl.nchunk[g] > 1;
         const int row = m * kTileM + r_in_tile;
         const bool valid = row < p.M;
         for (int cc = part * cols_per_part; cc < (part + 1) * cols_per_part; cc += 32) {
@@ -624,16 +683,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_32cols(taddr + cc, ra);
           tmem_ld_wait();
           if (!valid) continue;
-          const bool second = col >= p.n_split;
-          float* base = routed ? (second ? p.w_b : p.w_a) : (second ? p.ws_b : p.ws_a);
-          const int ncols = second ? p.N - p.n_split : p.n_split;
-          const int c0 = second ? col - p.n_split : col;
-          float* dst = base + (routed ? static_cast<size_t>(g) * p.M * ncols : 0) +
-                       static_cast<size_t>(row) * ncols + c0;
+          float* dst;
+          if (split) {
+            dst = p.part + (static_cast<size_t>(ctl.pslot[g] + ti.c) * p.M + row) * p.N + col;
+          } else {
+            const bool second = col >= p.n_split;
+            float* base = routed ? (second ? p.w_b : p.w_a) : (second ? p.ws_b : p.ws_a);
+            const int ncols = second ? p.N - p.n_split : p.n_split;
+            const int c0 = second ? col - p.n_split : col;
+            dst = base + (routed ? static_cast<size_t>(g) * p.M * ncols : 0) + static_cast<size_t>(row) * ncols + c0;
+          }
           float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
-            if (nkb == 0)
+            if (empty_k)
               d4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
             else
               d4[v] = make_float4(__uint_as_float(ra[4 * v]), __uint_as_float(ra[4 * v + 1]),
@@ -655,6 +718,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     tmem_dealloc_pair(tmem_base, kTmemCols);
   }
+}
+
+// Weight gradients of the split groups: the chunk partials of group g added
+// in chunk order, split by column into the two outputs.  Block (x, g) covers
+// 1024 consecutive floats of [M, N].
+__global__ void __launch_bounds__(256) wgrad_reduce_kernel(const float* __restrict__ part,
+                                                           const int32_t* __restrict__ offsets, int E,
+                                                           int T_shared, int M, int N, int n_split,
+                                                           float* w_a, float* w_b, float* ws_a, float* ws_b) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int g = blockIdx.y;
+  auto nchunk = [&](int h) {
+    const int rows = h < E ? ((offsets[h + 1] - offsets[h] + 63) & ~63) : T_shared;
+    const int nkb = (rows + kBK - 1) / kBK;
+    return max(1, (nkb + kMaxChunkKb - 1) / kMaxChunkKb);
+  };
+  const int nc = nchunk(g);
+  if (nc <= 1) return;
+  int slot = 0;
+  for (int h = 0; h < g; ++h) {
+    const int c = nchunk(h);
+    slot += c > 1 ? c : 0;
+  }
+  const size_t mn = static_cast<size_t>(M) * N;
+  const size_t i4 = (static_cast<size_t>(blockIdx.x) * 256 + threadIdx.x) * 4;
+  if (i4 >= mn) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = 0; c < nc; ++c) {
+    const float4 v = *reinterpret_cast<const float4*>(part + (slot + c) * mn + i4);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  const int row = static_cast<int>(i4 / N), col = static_cast<int>(i4 % N);
+  const bool routed = g < E;
+  const bool second = col >= n_split;
+  float* base = routed ? (second ? w_b : w_a) : (second ? ws_b : ws_a);
+  const int ncols = second ? N - n_split : n_split;
+  const int c0 = second ? col - n_split : col;
+  *reinterpret_cast<float4*>(base + (routed ? static_cast<size_t>(g) * M * ncols : 0) +
+                             static_cast<size_t>(row) * ncols + c0) = acc;
 }
 
 // Per-device launch state: co-resident CTA pairs per mode, error word address.
@@ -748,6 +854,13 @@ BwdArgs base_args(const BwdLayout& L, const int32_t* offsets) {
 
 int bwd_padded_rows(const moe_dims& d) { return d.T * d.k + 64 * d.E; }
 
+size_t bwd_wgrad_part_floats(const moe_dims& d, bool shared) {
+  // a split group has nchunk < 2 nkb / kMaxChunkKb chunks
+  const size_t kb = (static_cast<size_t>(d.T) * d.k + 64 * d.E) / kBK + (shared ? (d.T + kBK - 1) / kBK : 0);
+  const size_t slots = kb / (kMaxChunkKb / 2) + 2;
+  return slots * 2 * static_cast<size_t>(d.D) * d.F;
+}
+
 cudaError_t launch_bwd_dgrad_w2(const BwdLayout& L, const int32_t* offsets, const uint16_t* ybar,
                                 const uint16_t* d_out, const uint16_t* W2, const uint16_t* Ws2,
                                 uint16_t* hbar, cudaStream_t s, bool pdl) {
@@ -798,7 +911,11 @@ cudaError_t launch_bwd_act(const BwdLayout& L, const int32_t* offsets, const uin
   }
   const uint64_t rows = static_cast<uint64_t>(L.S_pad) + (L.shared ? d.T : 0);
   if ((e = tensor_map_2d(&m[6], gu, rows, 2 * d.F, kOutBoxRows, kOutBoxCols)) != cudaSuccess) return e;
-  if ((e = tensor_map_2d(&m[7], h, rows, d.F, kOutBoxRows, kOutBoxCols)) != cudaSuccess) return e;
+  if (h != nullptr) {
+    if ((e = tensor_map_2d(&m[7], h, rows, d.F, kOutBoxRows, kOutBoxCols)) != cudaSuccess) return e;
+  } else {
+    m[7] = m[6];
+  }
   BwdArgs a = base_args(L, offsets);
   a.K = d.D;
   a.N = d.F;
@@ -842,7 +959,7 @@ cudaError_t launch_bwd_dgrad_x(const BwdLayout& L, const int32_t* offsets, const
 cudaError_t launch_bwd_wgrad(const BwdLayout& L, const int32_t* offsets, const uint16_t* A,
                              int a_padded, int M, const uint16_t* A_sh, const uint16_t* B, int N,
                              const uint16_t* B_sh, int n_split, float* w_a, float* w_b, float* ws_a,
-                             float* ws_b, cudaStream_t s, bool pdl) {
+                             float* ws_b, float* part, cudaStream_t s, bool pdl) {
   const moe_dims& d = L.d;
   const int S = d.T * d.k;
   CUtensorMap m[8];
@@ -868,8 +985,14 @@ cudaError_t launch_bwd_wgrad(const BwdLayout& L, const int32_t* offsets, const u
   a.w_b = w_b;
   a.ws_a = ws_a;
   a.ws_b = ws_b;
+  a.part = part;
   m[7] = m[6];
-  return launch_mode<kWgrad>(m, a, s, pdl);
+  e = launch_mode<kWgrad>(m, a, s, pdl);
+  if (e != cudaSuccess) return e;
+  const size_t mn4 = (static_cast<size_t>(M) * N / 4 + 255) / 256;
+  const dim3 grid(static_cast<unsigned>(mn4), d.E + (L.shared ? 1 : 0));
+  return launch_kernel(wgrad_reduce_kernel, grid, dim3(256), 0, s, true, static_cast<const float*>(part), offsets,
+                       d.E, L.shared ? d.T : 0, M, N, n_split, w_a, w_b, ws_a, ws_b);
 }
 
 }  // namespace moe

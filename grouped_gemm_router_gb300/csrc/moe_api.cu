@@ -73,6 +73,7 @@ struct BwdWorkspace {
   float* lbar;     // [T, k]
   float* rpart;    // router-gradient partials
   uint16_t* wgt;   // Wg^T [E, D]
+  float* wpart;    // weight-gradient partial sums of split groups
   size_t bytes;
 };
 
@@ -96,6 +97,7 @@ BwdWorkspace carve_bwd(void* base, const moe_dims& d, bool shared) {
   w.lbar = reinterpret_cast<float*>(take(S * 4));
   w.rpart = reinterpret_cast<float*>(take(bwd_router_part_floats(d) * 4));
   w.wgt = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(d.E) * d.D * 2));
+  w.wpart = reinterpret_cast<float*>(take(bwd_wgrad_part_floats(d, shared) * 4));
   w.bytes = off;
   return w;
 }
@@ -200,6 +202,10 @@ moe_status run_backward(const uint16_t* x, const uint16_t* Wg, const uint16_t* W
   const float* w = routed_in ? o->weights_in : fw.w;
   const BwdLayout L{d, shared, bwd_padded_rows(d)};
   const size_t Sp = static_cast<size_t>(L.S_pad);
+  const size_t S = static_cast<size_t>(d.T) * d.k;
+  // The unchained forward left h in its workspace (the recompute gives the
+  // same bits); after a chained forward the recompute stores h itself.
+  const bool fwd_h = o == nullptr || (o->flags & MOE_FFN_CHAINED) == 0;
   cudaError_t e;
   record(o, 0, s);
   e = launch_combine_bwd(L, d_out, fw.y, w, ids, fw.inv, fw.offsets, routed_in ? 1 : 0, bw.ybar, bw.wbar,
@@ -209,18 +215,20 @@ moe_status run_backward(const uint16_t* x, const uint16_t* Wg, const uint16_t* W
   e = launch_bwd_dgrad_w2(L, fw.offsets, bw.ybar, d_out, W2, Ws2, bw.hbar, s, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(o, 2, s);
-  e = launch_bwd_act(L, fw.offsets, fw.x_sorted, x, W1, W3, Ws1, Ws3, bw.hbar, bw.gu, bw.h, s, true);
+  e = launch_bwd_act(L, fw.offsets, fw.x_sorted, x, W1, W3, Ws1, Ws3, bw.hbar, bw.gu, fwd_h ? nullptr : bw.h,
+                     s, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(o, 3, s);
   e = launch_bwd_dgrad_x(L, fw.offsets, bw.gu, W1, W3, Ws1, Ws3, bw.xbar, s, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(o, 4, s);
   e = launch_bwd_wgrad(L, fw.offsets, fw.x_sorted, 0, d.D, x, bw.gu, 2 * d.F, bw.gu + Sp * 2 * d.F, d.F,
-                       dW1, dW3, dWs1, dWs3, s, true);
+                       dW1, dW3, dWs1, dWs3, bw.wpart, s, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(o, 5, s);
-  e = launch_bwd_wgrad(L, fw.offsets, bw.h, 1, d.F, bw.h + Sp * d.F, bw.ybar, d.D, d_out, d.D, dW2,
-                       nullptr, dWs2, nullptr, s, true);
+  e = launch_bwd_wgrad(L, fw.offsets, fwd_h ? fw.h : bw.h, fwd_h ? 0 : 1, d.F,
+                       fwd_h ? fw.h + S * d.F : bw.h + Sp * d.F, bw.ybar, d.D, d_out, d.D, dW2, nullptr, dWs2,
+                       nullptr, bw.wpart, s, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(o, 6, s);
   e = launch_dx_gather(L, bw.xbar, ids, fw.inv, fw.offsets, routed_in ? nullptr : bw.lbar, bw.wgt, dx,
@@ -268,7 +276,7 @@ moe_status moe_ffn_backward(const void* x, const void* Wg, const void* W1, const
     if (p != nullptr && !aligned16(p)) return MOE_ERR_INVALID_ARG;
   if (opts != nullptr && ((opts->ids_in == nullptr) != (opts->weights_in == nullptr)))
     return MOE_ERR_INVALID_ARG;
-  if (opts != nullptr && opts->flags != 0) return MOE_ERR_INVALID_ARG;
+  if (opts != nullptr && (opts->flags & ~MOE_FFN_CHAINED) != 0) return MOE_ERR_INVALID_ARG;
   const bool shared = sh == 1;
   const Workspace fw = carve(const_cast<void*>(fwd_workspace), d, shared, false);
   if (fwd_ws_bytes < fw.bytes) return MOE_ERR_WORKSPACE;

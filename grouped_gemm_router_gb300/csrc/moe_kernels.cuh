@@ -97,11 +97,14 @@ cudaError_t launch_bwd_act(const BwdLayout& L, const int32_t* offsets, const uin
 cudaError_t launch_bwd_dgrad_x(const BwdLayout& L, const int32_t* offsets, const uint16_t* gu,
                                const uint16_t* W1, const uint16_t* W3, const uint16_t* Ws1,
                                const uint16_t* Ws3, uint16_t* xbar, cudaStream_t s, bool pdl);
-// C[e] = A[rows_e]^T B[rows_e] in fp32, columns [0, n_split) to w_a, the rest to w_b.
+// C[e] = A[rows_e]^T B[rows_e] in fp32, columns [0, n_split) to w_a, the rest
+// to w_b.  Long groups are split along the rows; their partials go to `part`
+// (bwd_wgrad_part_floats floats) and a second launch adds them in order.
+size_t bwd_wgrad_part_floats(const moe_dims& d, bool shared);
 cudaError_t launch_bwd_wgrad(const BwdLayout& L, const int32_t* offsets, const uint16_t* A,
                              int a_padded, int M, const uint16_t* A_sh, const uint16_t* B, int N,
                              const uint16_t* B_sh, int n_split, float* w_a, float* w_b, float* ws_a,
-                             float* ws_b, cudaStream_t s, bool pdl);
+                             float* ws_b, float* part, cudaStream_t s, bool pdl);
 // Combine backward: y_bar (padded layout, padding rows zeroed), the gradient of
 // the gate weights and of the selected logits (zero when routed_in).
 // Also writes Wg^T [E, D] into wgt (unless routed_in).

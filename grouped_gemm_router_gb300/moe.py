@@ -202,10 +202,11 @@ def padded_rows(counts):
 
 def moe_ffn_backward(x, Wg, W1, W3, W2, k, d_out, workspace: Workspace, Ws1=None, Ws3=None, Ws2=None,
                      bwd_workspace: BackwardWorkspace | None = None, ids_in=None, weights_in=None,
-                     router=True, stage_events=None):
+                     router=True, stage_events=None, chained=False):
     """Gradients of sum(d_out * out) for the forward call that filled
     `workspace`.  Returns dict(dx bf16 [T, D], dW1, dW3 [E, D, F], dW2 [E, F, D]
-    (+ dWs1, dWs3, dWs2), and with router=True dWg [D, E], dbias [E]) fp32."""
+    (+ dWs1, dWs3, dWs2), and with router=True dWg [D, E], dbias [E]) fp32.
+    chained: the forward call ran with chained=True (its workspace has no h)."""
     T, D, F, E, k = layer_dims(x, W1, k)
     shared = Ws1 is not None
     _need(d_out, "d_out", torch.bfloat16, (T, D))
@@ -224,7 +225,7 @@ def moe_ffn_backward(x, Wg, W1, W3, W2, k, d_out, workspace: Workspace, Ws1=None
                               _ptr(g["dx"]), _ptr(g.get("dWg")), _ptr(g.get("dbias")), _ptr(g["dW1"]),
                               _ptr(g["dW3"]), _ptr(g["dW2"]), _ptr(g.get("dWs1")), _ptr(g.get("dWs3")),
                               _ptr(g.get("dWs2")), _ptr(bwd_workspace.buf), bwd_workspace.nbytes,
-                              _options(stage_events, ids_in, weights_in), _stream())
+                              _options(stage_events, ids_in, weights_in, chained), _stream())
     check(st, "moe_ffn_backward")
     return g
 

@@ -136,7 +136,9 @@ moe_status moe_ffn_forward_host(const void* x_host, const void* Wg, const float*
  * h [R, F], x_bar [R, D] (bf16, the routed rows of each expert padded to a
  * multiple of 64 rows in expert order, the shared rows from S_pad), the
  * gate-weight and selected-logit gradients [T, k] fp32, the router-
- * gradient partials ((T*k/256 + E) * (D + 1) fp32) and Wg^T [E, D] bf16.
+ * gradient partials ((T*k/64 + E) * (D + 1) fp32), Wg^T [E, D] bf16 and
+ * the weight-gradient partial sums of groups split along their rows
+ * ((kb / 80 + 2) * 2 * D * F fp32, kb = (T*k + 64 E) / 64 (+ ceil(T / 64))).
  * 0 for unsupported dimensions. */
 size_t moe_ffn_backward_workspace_size(moe_dims d, int has_shared);
 
@@ -162,7 +164,10 @@ size_t moe_ffn_backward_workspace_size(moe_dims d, int has_shared);
  *   the router term of dx are zero / skipped); stage_events [0..8] are
  *   recorded before the combine backward, after it, after h_bar, after
  *   g_bar|u_bar, after x_bar, after dW1|dW3, after dW2, after dx and after
- *   the router gradient; flags must be 0.
+ *   the router gradient; flags: MOE_FFN_CHAINED if the forward call ran
+ *   chained (its workspace then holds no h, and the backward stores the
+ *   recomputed h in its own workspace), else 0 (the W2 gradient reads the
+ *   forward's h).
  *   Precision: fp32 accumulation everywhere; y_bar, h_bar, g_bar, u_bar, h
  *   and x_bar are stored as bf16 between the GEMMs; dx is summed in fp32 and
  *   rounded once.  Deterministic (no atomics). */

@@ -121,8 +121,8 @@ def test_backward_argument_validation_before_launch(native):
     assert bwd_call(ws_bytes=bws - 1) == N.MOE_ERR_WORKSPACE
     assert bwd_call(d=N.dims(256, 100, 256, 4, 2)) == N.MOE_ERR_UNSUPPORTED_SHAPE
     o = N.MoeOptions()
-    o.flags = N.MOE_FFN_CHAINED
-    assert bwd_call(opts=o) == N.MOE_ERR_INVALID_ARG                      # no flags in the backward
+    o.flags = 2
+    assert bwd_call(opts=o) == N.MOE_ERR_INVALID_ARG                      # no such flag
     assert N.lib.moe_launch_count() == 0
 
 
@@ -133,7 +133,9 @@ def test_backward_workspace_size_matches_documented_layout(native):
         Sp = S + 64 * E
         R = Sp + (T if sh else 0)
         n = a(Sp * D * 2) + a(R * F * 2) + a(R * F * 4) + a(R * F * 2) + a(R * D * 2) + 2 * a(S * 4)
-        n += a((S // 256 + E) * (D + 1) * 4) + a(E * D * 2)
+        n += a((S // 64 + E) * (D + 1) * 4) + a(E * D * 2)
+        kb = (S + 64 * E) // 64 + ((T + 63) // 64 if sh else 0)     # weight-gradient partial slots
+        n += a((kb // 80 + 2) * 2 * D * F * 4)
         assert native.lib.moe_ffn_backward_workspace_size(native.dims(T, D, F, E, k), sh) == n
 
 

@@ -16,8 +16,9 @@ between its GEMMs (relative rounding 2^-9 each) and accumulates in fp32:
 Stage checks feed the oracle the GPU's own bf16 intermediates (read from
 the backward workspace), so each GEMM is held to its fp32 accumulation:
 h_bar, x_bar: 1e-4 + 4e-3 |ref|; g_bar | u_bar: 2e-3 rms + 8e-3 |ref|; weight
-gradients: 1e-3 rms + 1e-3 |ref|; and the recomputed h equals the forward's
-h bit for bit (same kernel arithmetic).
+gradients: 1e-3 rms + 1e-3 |ref|; and the h the backward recomputes after a
+chained forward equals the unchained forward's h bit for bit (same kernel
+arithmetic).
 Routing: the small cases use seeds whose top-k margins all exceed 1e-3 (the
 router's selection is then the oracle's, and the router gradients are
 compared); the full-size case fixes the routing from outside (no router
@@ -73,7 +74,8 @@ def _run(moe, L, k, d_out_bits, shared, chained=False, ids_in=None, weights_in=N
     out = moe.moe_ffn_forward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], k, bias=G["bias"], workspace=ws,
                               ids_in=ids_in, weights_in=weights_in, chained=chained, **kw)
     g = moe.moe_ffn_backward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], k, to_dev(d_out_bits), ws,
-                             bwd_workspace=bws, ids_in=ids_in, weights_in=weights_in, router=router, **kw)
+                             bwd_workspace=bws, ids_in=ids_in, weights_in=weights_in, router=router,
+                             chained=chained, **kw)
     torch.cuda.synchronize()
     assert moe.device_error() == 0
     return out, g, (ws, bws)
@@ -94,9 +96,8 @@ def _stage_checks(moe, L, k, d_out, g, wss, shared):
     W1, W3, W2 = (orc.bf16_to_f64(L[n]) for n in ("W1", "W3", "W2"))
     xs = to_f64(V["x_sorted"])
     ybar, hbar = to_f64(B["ybar"][prow]), to_f64(B["hbar"][prow])
-    gu, hbw, xbar = to_f64(B["gu"][prow]), B["h"][prow], to_f64(B["xbar"][prow])
-    # the recomputed h is the forward's h, bit for bit
-    assert torch.equal(hbw, V["h"][:S]), "recomputed h differs from the forward's h"
+    gu, xbar = to_f64(B["gu"][prow]), to_f64(B["xbar"][prow])
+    hbw = V["h"][:S]  # the W2 gradient reads the forward's h
     for e in range(E):
         a, b = int(offs[e]), int(offs[e + 1])
         if a == b:
@@ -139,7 +140,7 @@ def _stage_checks(moe, L, k, d_out, g, wss, shared):
         assert_close(hb_s, d64 @ Ws2.T, "h_bar shared", atol=H_ATOL, rtol=H_RTOL)
         assert_wgrad(to_f64(g["dWs1"]), x64.T @ gu_s[:, :F], "dWs1 (GPU g_bar)", 1e-3, 1e-3)
         assert_wgrad(to_f64(g["dWs3"]), x64.T @ gu_s[:, F:], "dWs3 (GPU u_bar)", 1e-3, 1e-3)
-        assert_wgrad(to_f64(g["dWs2"]), to_f64(B["h"][Sp:Sp + T]).T @ d64, "dWs2 (GPU h)", 1e-3, 1e-3)
+        assert_wgrad(to_f64(g["dWs2"]), to_f64(V["h"][S:S + T]).T @ d64, "dWs2 (GPU h)", 1e-3, 1e-3)
 
 
 CASES = [
@@ -152,6 +153,7 @@ CASES = [
     (64, 64, 64, 16, 4, True, 44, None),               # tiny groups
     (1, 64, 128, 2, 2, True, 45, None),                # one token
     (1100, 384, 512, 4, 1, True, 46, None),            # top-1, several tiles per group
+    (12000, 128, 192, 1, 1, True, 49, None),           # routed and shared groups split along their rows
 ]
 
 
@@ -181,10 +183,15 @@ def test_backward_after_chained_forward_and_deterministic(moe):
     T, D, F, E, k = 512, 128, 256, 4, 2
     _, L = inputs.make_custom(T, D, F, E, k, True, 47)
     d_out = _d_out(T, D, 47)
-    _, g1, _ = _run(moe, L, k, d_out, True)
-    _, g2, _ = _run(moe, L, k, d_out, True, chained=True)
+    _, g1, (ws1, _) = _run(moe, L, k, d_out, True)
+    _, g2, (_, bws2) = _run(moe, L, k, d_out, True, chained=True)
     for n in g1:
         assert torch.equal(g1[n], g2[n]), n
+    # after the chained forward the backward recomputed h itself: the forward's bits
+    V, B = ws1.views(), bws2.views()
+    prow = torch.tensor(moe.padded_rows(V["counts"].cpu().numpy()), dtype=torch.long, device="cuda")
+    assert torch.equal(B["h"][prow], V["h"][:T * k]), "recomputed h differs from the forward's h"
+    assert torch.equal(B["h"][B["S_pad"]:B["S_pad"] + T], V["h"][T * k:T * k + T])
 
 
 def test_backward_fixed_routing_skips_router(moe):
