@@ -79,6 +79,90 @@ __global__ void __launch_bounds__(256) pack_router_weights_kernel(const uint16_t
 // 32K-token batch (512 blocks) fit in one wave for E <= 8.
 constexpr int route_min_blocks(int nt) { return nt <= 1 ? 4 : nt <= 2 ? 3 : nt <= 8 ? 2 : 1; }
 
+// Top-k + softmax of the logits a quad holds for rows row0 (r = 0) and row1
+// (r = 1): thread (g, c) has experts 8n + 2c + {0, 1} in acc[n][2r + {0, 1}].
+// Each of the k rounds takes the largest not-yet-chosen logit across the
+// quad (ties to the lower expert index; NaN counts as -inf); the softmax is
+// over the k selected logits.  Writes ids / wts of rows < T and counts the
+// selections in s_hist.
+template <int NT, int KMAX>
+MOE_DEV void select_topk(const float (&acc)[NT][4], int row0, int row1, int c, int T, int E, int k,
+                         const float* __restrict__ bias, int32_t* __restrict__ ids, float* __restrict__ wts,
+                         int* s_hist) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int row = r ? row1 : row0;
+    float v[2 * NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = n * 8 + 2 * c + h;
+        float l = acc[n][2 * r + h];
+        if (bias != nullptr && e < E) l += bias[e];
+        if (isnan(l)) l = -INFINITY;
+        v[2 * n + h] = l;
+      }
+    }
+    uint32_t taken = 0;
+    float sel_v[KMAX];
+    int sel_e[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      sel_v[j] = 0.f;
+      sel_e[j] = 0;
+      if (j < k) {
+        float best = -INFINITY;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < 2 * NT; ++i) {
+          const int e = (i >> 1) * 8 + 2 * c + (i & 1);
+          if (e < E && !((taken >> i) & 1u) && (v[i] > best || (v[i] == best && e < be))) {
+            best = v[i];
+            be = e;
+          }
+        }
+#pragma unroll
+        for (int off = 1; off <= 2; off <<= 1) {
+          const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+          if (ob > best || (ob == best && oe < be)) {
+            best = ob;
+            be = oe;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 2 * NT; ++i) {
+          const int e = (i >> 1) * 8 + 2 * c + (i & 1);
+          if (e == be) taken |= 1u << i;
+        }
+        sel_v[j] = best;
+        sel_e[j] = be;
+      }
+    }
+    float z[KMAX];
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      z[j] = 0.f;
+      if (j < k) {
+        z[j] = expf(sel_v[j] - sel_v[0]);
+        sum += z[j];
+      }
+    }
+    if (row < T) {
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (j < k && (j & 3) == c) {
+          ids[static_cast<size_t>(row) * k + j] = sel_e[j];
+          wts[static_cast<size_t>(row) * k + j] = z[j] / sum;
+          atomicAdd(&s_hist[sel_e[j]], 1);
+        }
+      }
+    }
+  }
+}
+
 // Block = 8 warps for TB = 16 MT tokens (MT = 1, 2 or 4 tiles of 16 tokens).
 // Warp w computes tile w % MT over the 32-wide D-chunks kc with
 // kc % DS == w / MT (DS = 8 / MT warps share a tile), loading x and the packed
@@ -168,79 +252,7 @@ __global__ void __launch_bounds__(kRouteThreads, route_min_blocks(NT)) route_ker
       for (int i = 0; i < 4; ++i) acc[n][i] += red[((w2 * NT + n) * 4 + i) * 32 + lane];
   }
 
-  // ---- top-k + softmax for rows g (r = 0) and g + 8 (r = 1) ----
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int row = r ? row1 : row0;
-    float v[2 * NT];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int e = n * 8 + 2 * c + h;
-        float l = acc[n][2 * r + h];
-        if (bias != nullptr && e < E) l += bias[e];
-        if (isnan(l)) l = -INFINITY;
-        v[2 * n + h] = l;
-      }
-    }
-    uint32_t taken = 0;
-    float sel_v[KMAX];
-    int sel_e[KMAX];
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      sel_v[j] = 0.f;
-      sel_e[j] = 0;
-      if (j < k) {
-        float best = -INFINITY;
-        int be = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < 2 * NT; ++i) {
-          const int e = (i >> 1) * 8 + 2 * c + (i & 1);
-          if (e < E && !((taken >> i) & 1u) && (v[i] > best || (v[i] == best && e < be))) {
-            best = v[i];
-            be = e;
-          }
-        }
-#pragma unroll
-        for (int off = 1; off <= 2; off <<= 1) {
-          const float ob = __shfl_xor_sync(0xffffffffu, best, off);
-          const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-          if (ob > best || (ob == best && oe < be)) {
-            best = ob;
-            be = oe;
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 2 * NT; ++i) {
-          const int e = (i >> 1) * 8 + 2 * c + (i & 1);
-          if (e == be) taken |= 1u << i;
-        }
-        sel_v[j] = best;
-        sel_e[j] = be;
-      }
-    }
-    float z[KMAX];
-    float sum = 0.f;
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      z[j] = 0.f;
-      if (j < k) {
-        z[j] = expf(sel_v[j] - sel_v[0]);
-        sum += z[j];
-      }
-    }
-    if (row < T) {
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        if (j < k && (j & 3) == c) {
-          ids[static_cast<size_t>(row) * k + j] = sel_e[j];
-          wts[static_cast<size_t>(row) * k + j] = z[j] / sum;
-          atomicAdd(&s_hist[sel_e[j]], 1);
-        }
-      }
-    }
-  }
+  select_topk<NT, KMAX>(acc, row0, row1, c, T, E, k, bias, ids, wts, s_hist);
   // only the MT selecting warps are left: sync them on a named barrier
   asm volatile("bar.sync 1, %0;" ::"r"(MT * 32) : "memory");
   if (hist != nullptr)
