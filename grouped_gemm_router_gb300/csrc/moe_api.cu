@@ -264,6 +264,7 @@ moe_status moe_ffn_backward(const void* x, const void* Wg, const void* W1, const
                             void* stream) {
   moe_status st = check_dims(d);
   if (st != MOE_OK) return st;
+  if (d.T == 0) return MOE_OK;  // nothing to differentiate (the gradient tensors are left as given)
   if (!x || !Wg || !W1 || !W3 || !W2 || !d_out || !fwd_workspace || !dx || !dW1 || !dW3 || !dW2 ||
       !workspace)
     return MOE_ERR_INVALID_ARG;

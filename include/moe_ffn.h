@@ -170,7 +170,8 @@ size_t moe_ffn_backward_workspace_size(moe_dims d, int has_shared);
  *   forward's h).
  *   Precision: fp32 accumulation everywhere; y_bar, h_bar, g_bar, u_bar, h
  *   and x_bar are stored as bf16 between the GEMMs; dx is summed in fp32 and
- *   rounded once.  Deterministic (no atomics). */
+ *   rounded once.  Deterministic (no atomics).  T = 0 returns MOE_OK without
+ *   touching any buffer. */
 moe_status moe_ffn_backward(const void* x, const void* Wg, const void* W1, const void* W3,
                             const void* W2, const void* Ws1, const void* Ws3, const void* Ws2,
                             const void* d_out, moe_dims d, const void* fwd_workspace,

@@ -251,3 +251,28 @@ def test_backward_full_size_sampled(moe, name):
             assert_wgrad(to_f64(g["dW3"][e][:, f]), xs.T @ ub, f"dW3[{e}][:, {f}]")
             hcol = orc.silu(gcol) * ucol
             assert_wgrad(to_f64(g["dW2"][e][f, :]), hcol @ ybar, f"dW2[{e}][{f}, :]")
+
+
+def test_backward_widest_router_fixed_routing(moe):
+    """E = 128 experts (most of them with a handful of rows, some empty) and
+    the largest top-k, with the routing fixed from outside."""
+    T, D, F, E, k = 300, 128, 128, 128, 16
+    _, L = inputs.make_custom(T, D, F, E, k, True, 50)
+    ids, w = orc.topk_softmax(orc.router_logits(orc.bf16_to_f64(L["x"]), orc.bf16_to_f64(L["Wg"])), k)
+    d_out = _d_out(T, D, 50)
+    _, g, _ = _run(moe, L, k, d_out, True, ids_in=to_dev(ids.astype(np.int32)),
+                   weights_in=to_dev(w.astype(np.float32)), router=False)
+    ref = bwd.moe_ffn_backward(L["x"], L["Wg"], L["W1"], L["W3"], L["W2"], k, d_out, Ws1=L["Ws1"],
+                               Ws3=L["Ws3"], Ws2=L["Ws2"], ids=ids, weights=w)
+    assert_dx(to_f64(g["dx"]), ref["dx"])
+    for n in ("dW1", "dW3", "dW2", "dWs1", "dWs3", "dWs2"):
+        assert_wgrad(to_f64(g[n]), ref[n], n)
+
+
+def test_backward_zero_tokens_is_a_no_op(moe):
+    _, L = inputs.make_custom(4, 64, 64, 2, 1, False, 51)
+    G = {key: (to_dev(v) if v is not None else None) for key, v in L.items()}
+    ws = moe.Workspace(0, 64, 64, 2, 1, False)
+    x0 = G["x"][:0]
+    g = moe.moe_ffn_backward(x0, G["Wg"], G["W1"], G["W3"], G["W2"], 1, x0, ws)
+    assert g["dx"].shape == (0, 64)
