@@ -232,11 +232,14 @@ MOE_DEV bool chunk_of(const int32_t* offsets, int E, int c, int* e_out, int* r0,
   return false;
 }
 
+// Block (chunk, column block): thread (h, c) adds rows h, h + 2, ... of the
+// chunk for 8-column group c; the two halves are added in order h = 0, 1.
 __global__ void __launch_bounds__(kBwdThreads) router_bwd_partial_kernel(
     const uint4* __restrict__ x_sorted, const int32_t* __restrict__ perm, const float* __restrict__ lbar,
     const int32_t* __restrict__ offsets, int E, int D, float* __restrict__ part,
     float* __restrict__ part_bias) {
   __shared__ float lw[kRouterRows];
+  __shared__ float4 half1[kBwdThreads / 2][2];
   griddep_wait();
   griddep_launch_dependents();
   int e, r0, r1;
@@ -245,14 +248,16 @@ __global__ void __launch_bounds__(kBwdThreads) router_bwd_partial_kernel(
   for (int i = threadIdx.x; i < n; i += blockDim.x) lw[i] = lbar[perm[r0 + i]];
   __syncthreads();
   const int n16 = D >> 3;
-  const int c = blockIdx.y * blockDim.x + threadIdx.x;  // 8-column group
-  if (c < n16) {
-    float acc[8];
+  const int cols = blockDim.x / 2;  // 8-column groups per block
+  const int h = threadIdx.x / cols, tc = threadIdx.x % cols;
+  const int c = blockIdx.y * cols + tc;
+  float acc[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  if (c < n16) {
     const uint4* col = x_sorted + static_cast<size_t>(r0) * n16 + c;
 #pragma unroll 8
-    for (int r = 0; r < n; ++r) {
+    for (int r = h; r < n; r += 2) {
       const uint4 v = __ldg(col + static_cast<size_t>(r) * n16);
       const float l = lw[r];
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -262,9 +267,17 @@ __global__ void __launch_bounds__(kBwdThreads) router_bwd_partial_kernel(
         acc[2 * q + 1] = fmaf(l, bf16_hi(u[q]), acc[2 * q + 1]);
       }
     }
+  }
+  if (h == 1) {
+    half1[tc][0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    half1[tc][1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+  __syncthreads();
+  if (h == 0 && c < n16) {
+    const float4 p0 = half1[tc][0], p1 = half1[tc][1];
     float4* dst = reinterpret_cast<float4*>(part + static_cast<size_t>(blockIdx.x) * D + 8 * c);
-    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    dst[0] = make_float4(acc[0] + p0.x, acc[1] + p0.y, acc[2] + p0.z, acc[3] + p0.w);
+    dst[1] = make_float4(acc[4] + p1.x, acc[5] + p1.y, acc[6] + p1.z, acc[7] + p1.w);
   }
   if (blockIdx.y == 0 && threadIdx.x < 32) {
     float sb = 0.f;
@@ -274,27 +287,46 @@ __global__ void __launch_bounds__(kBwdThreads) router_bwd_partial_kernel(
   }
 }
 
-// dWg[d][e] and dbias[e]: expert e's chunk partials added in chunk order.
-__global__ void router_bwd_reduce_kernel(const float* __restrict__ part, const float* __restrict__ part_bias,
-                                         const int32_t* __restrict__ offsets, int D, int E,
-                                         float* __restrict__ dWg, float* __restrict__ dbias) {
+// dWg[d][e] and dbias[e]: expert e's chunk partials added in a fixed order.
+// Block (column block, e): 4 x 64 threads; quarter j of the threads adds the
+// chunks j, j + 4, ... of expert e for its column, the four sums are then
+// added in order j = 0..3 (column block 0 also adds the bias partials).
+constexpr int kRedCols = 64;
+constexpr int kRedSplit = 4;
+
+__global__ void __launch_bounds__(kRedCols * kRedSplit) router_bwd_reduce_kernel(
+    const float* __restrict__ part, const float* __restrict__ part_bias, const int32_t* __restrict__ offsets,
+    int D, int E, float* __restrict__ dWg, float* __restrict__ dbias) {
+  __shared__ float sums[kRedSplit][kRedCols + 1];
   griddep_wait();
   griddep_launch_dependents();
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  const bool bias_item = i >= D * E;
-  if (i >= D * E + E) return;
-  const int e = bias_item ? i - D * E : i % E;
-  const int d = bias_item ? 0 : i / E;
+  const int e = blockIdx.y;
+  const int tc = threadIdx.x % kRedCols, j = threadIdx.x / kRedCols;
+  const int d = blockIdx.x * kRedCols + tc;
   int base = 0;
-  for (int g = 0; g < e; ++g)
-    base += (offsets[g + 1] - offsets[g] + kRouterRows - 1) / kRouterRows;
+  for (int g = 0; g < e; ++g) base += (offsets[g + 1] - offsets[g] + kRouterRows - 1) / kRouterRows;
   const int nc = (offsets[e + 1] - offsets[e] + kRouterRows - 1) / kRouterRows;
-  float s = 0.f;
-  for (int c = base; c < base + nc; ++c) s += bias_item ? part_bias[c] : part[static_cast<size_t>(c) * D + d];
-  if (bias_item) {
-    if (dbias != nullptr) dbias[e] = s;
-  } else if (dWg != nullptr) {
-    dWg[i] = s;
+  float s = 0.f, sb = 0.f;
+  if (d < D) {
+#pragma unroll 8
+    for (int c = j; c < nc; c += kRedSplit) s += part[static_cast<size_t>(base + c) * D + d];
+  }
+  if (blockIdx.x == 0 && tc == 0)
+    for (int c = j; c < nc; c += kRedSplit) sb += part_bias[base + c];
+  sums[j][tc] = s;
+  if (blockIdx.x == 0 && tc == 0) sums[j][kRedCols] = sb;
+  __syncthreads();
+  if (j == 0) {
+    float t = 0.f;
+#pragma unroll
+    for (int q = 0; q < kRedSplit; ++q) t += sums[q][tc];
+    if (d < D && dWg != nullptr) dWg[static_cast<size_t>(d) * E + e] = t;
+    if (blockIdx.x == 0 && tc == 0 && dbias != nullptr) {
+      float tb = 0.f;
+#pragma unroll
+      for (int q = 0; q < kRedSplit; ++q) tb += sums[q][kRedCols];
+      dbias[e] = tb;
+    }
   }
 }
 
@@ -337,18 +369,18 @@ cudaError_t launch_router_bwd(const BwdLayout& L, const uint16_t* x_sorted, cons
   const moe_dims& d = L.d;
   const int nch = router_chunks(d);
   float* part_bias = part + static_cast<size_t>(nch) * d.D;
-  // one thread per 8 columns, up to 256 threads per block
+  // two threads per 8 columns (each half of the chunk's rows), up to 256 threads per block
   const int n16 = d.D / 8;
-  const int threads = n16 >= kBwdThreads ? kBwdThreads : (n16 + 31) / 32 * 32;
-  const dim3 grid(nch, (n16 + threads - 1) / threads);
+  const int cols = n16 >= kBwdThreads / 2 ? kBwdThreads / 2 : (n16 + 15) / 16 * 16;
+  const int threads = 2 * cols;
+  const dim3 grid(nch, (n16 + cols - 1) / cols);
   cudaError_t e = launch_kernel(router_bwd_partial_kernel, grid, dim3(threads), 0, s, pdl,
                                 reinterpret_cast<const uint4*>(x_sorted), perm, lbar, offsets, d.E, d.D,
                                 part, part_bias);
   if (e != cudaSuccess) return e;
-  const int n = d.D * d.E + d.E;
-  return launch_kernel(router_bwd_reduce_kernel, dim3((n + 255) / 256), dim3(256), 0, s, pdl,
-                       static_cast<const float*>(part), static_cast<const float*>(part_bias), offsets, d.D,
-                       d.E, dWg, dbias);
+  return launch_kernel(router_bwd_reduce_kernel, dim3((d.D + kRedCols - 1) / kRedCols, d.E),
+                       dim3(kRedCols * kRedSplit), 0, s, pdl, static_cast<const float*>(part),
+                       static_cast<const float*>(part_bias), offsets, d.D, d.E, dWg, dbias);
 }
 
 }  // namespace moe
