@@ -197,6 +197,14 @@ def time_oracle(L, w, budget_s=12.0):
     return n * runs / total, n, runs, total
 
 
+def near_tie_tokens(L, w) -> int:
+    """Tokens whose k-th and (k+1)-th fp64 oracle logits differ by less than
+    1e-3: there either selection is correct (the parity tests' near-tie rule)."""
+    from oracle import moe_oracle as orc
+    logits = orc.router_logits(orc.bf16_to_f64(L["x"]), orc.bf16_to_f64(L["Wg"]), L["bias"])
+    return int((orc.topk_gap(logits, w.k) < 1e-3).sum())
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -624,7 +632,8 @@ def main():
         tps, n, runs, secs = time_oracle(L, w)
         cpu = {"value": tps, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
                "sample": f"{runs} runs of the first {n} of {w.T} tokens through the whole layer "
-                         f"({secs:.1f} s of fp64 numpy oracle)"}
+                         f"({secs:.1f} s of fp64 numpy oracle)",
+               "near_tie_tokens": near_tie_tokens(L, w)}
     line = {
         "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
