@@ -362,22 +362,6 @@ MOE_DEV uint32_t idesc_bf16_f32_ab(uint32_t M, uint32_t N, uint32_t a_mn_major, 
   return idesc_bf16_f32(M, N, b_mn_major) | (a_mn_major << 15);
 }
 
-// 16-byte global load through the read-only path with an L2 cache policy.
-MOE_DEV uint4 ldg_policy(const uint4* p, uint64_t policy) {
-  uint4 v;
-  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p), "l"(policy));
-  return v;
-}
-
-// 16-byte global store marked streaming (evict first): for data the next
-// kernels read once, so it does not push longer-lived lines out of L2.
-MOE_DEV void stg_streaming(uint4* p, const uint4& v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // Small helpers
 // ---------------------------------------------------------------------------

@@ -199,16 +199,14 @@ __global__ void __launch_bounds__(kRouteThreads, route_min_blocks(NT)) route_ker
   constexpr int KG = (NT >= 16) ? 1 : (NT >= 8) ? 2 : 4;  // chunks per load batch
   const int nkc = D >> 5;
   uint4 a0[KG], a1[KG];
-  // x stays in L2 for the permutation's gather (and the shared expert's A rows)
-  const uint64_t pol_x = l2_policy_evict_last();
   auto load_x = [&](int kc0) {  // x of one batch: 2 rows x KG chunks
 #pragma unroll
     for (int j = 0; j < KG; ++j) {
       const int kc = kc0 + j * DS;
       const bool in = kc < nkc;
       const int q = (kc << 2) + c;  // 16-byte column index
-      a0[j] = (ok0 && in) ? ldg_policy(xr0 + q, pol_x) : make_uint4(0, 0, 0, 0);
-      a1[j] = (ok1 && in) ? ldg_policy(xr1 + q, pol_x) : make_uint4(0, 0, 0, 0);
+      a0[j] = (ok0 && in) ? __ldg(xr0 + q) : make_uint4(0, 0, 0, 0);
+      a1[j] = (ok1 && in) ? __ldg(xr1 + q) : make_uint4(0, 0, 0, 0);
     }
   };
   // x does not come from the previous kernel (the weight packing): start
@@ -427,7 +425,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int cidx = c0 + 32 * u;
-          if (dst[r] != nullptr && cidx < n16) stg_streaming(dst[r] + cidx, v[r][u]);
+          if (dst[r] != nullptr && cidx < n16) dst[r][cidx] = v[r][u];
         }
     }
   }
