@@ -20,6 +20,10 @@
 // 256 rows with TMA starting at row0_g + 256 m; rows past the group belong to
 // the next group (or are zero-filled past the tensor) and are simply not
 // stored: the epilogue predicates each row (and each 32-column chunk past N).
+// When a group's last m-tile has at most 128 rows, the peer CTA loads no A
+// rows at all and its epilogue warps skip their TMEM reads: with many small
+// groups (64 experts of ~128 rows) that halves the A stream, the bottleneck
+// when the weights come from HBM.
 // The tile schedule is derived on the device from the offsets (no host
 // synchronisation): tiles are numbered group by group, n fastest, and pair c
 // takes tiles c, c + pairs, ...
@@ -44,9 +48,12 @@
 //     1024 bytes -> descriptor SBO = 1024; the k-th 16-wide slice starts
 //     32 k bytes into the tile.
 //   B tile 64 k x N/2 (N-major, straight from the [K, N] row-major weights):
-//     N/2 is split in 64-column boxes of 64 k-rows x 128 bytes (8 KB each);
+//     N/2 is split in 64-column blocks of 64 k-rows x 128 bytes (8 KB each);
 //     LBO = 8192 (next 64 columns), SBO = 1024 (next 8 k-rows); the k-th
-//     16-deep slice starts 2048 k bytes into the tile.
+//     16-deep slice starts 2048 k bytes into the tile.  One 3-D TMA box
+//     {64 columns, 64 rows, N/128 blocks} over the view {64, K rows, N / 64}
+//     (strides N * 2 and 128 bytes) lands the blocks in that order, so a
+//     k-block takes two TMA operations per CTA (A and B) instead of three.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -217,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_a = l2_policy_evict_normal();
       const uint64_t pol_b = l2_policy_evict_last();
-      const uint32_t pair_tx = 2u * static_cast<uint32_t>(kPairABytes + half_n * kBK * 2);
+      const uint32_t b_tx = 2u * static_cast<uint32_t>(half_n * kBK * 2);
       int stage = 0;
       uint32_t phase = 0;
       int g = 0;
@@ -231,6 +238,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* mA = routed ? &mapA : &mapA_sh;
         const int a_row = (routed ? ctl.row0[g] : p.shared_a_row0) + m * kPairBM + 128 * rank;
         const int b_row0 = routed ? g * p.K : 0;
+        // A tile whose rows all lie past the group's end (the peer's half of
+        // the last m-tile of a group of <= 128 more rows) is not loaded: those
+        // rows are never stored, so the MMA may read stale shared memory.
+        const bool peer_a = ctl.nrows[g] - m * kPairBM > 128;
+        const bool load_a = leader || peer_a;
+        const uint32_t pair_tx = b_tx + static_cast<uint32_t>(kPairABytes) * (peer_a ? 2u : 1u);
         // this CTA's B columns
         const CUtensorMap* mB;
         int bcol;
@@ -250,10 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = smem_base + stage * kPairStageBytes;
           const uint32_t sb = sa + kPairABytes;
           if (leader) mbar_arrive_expect_tx(smem_u32(&ctl.full[stage]), pair_tx);
-          tma_load_2d_pair(sa, mA, full_leader, kb * kBK, a_row, pol_a);
+          if (load_a) tma_load_2d_pair(sa, mA, full_leader, kb * kBK, a_row, pol_a);
           const int brow = b_row0 + kb * kBK;
-          for (int cch = 0; cch < half_n / 64; ++cch)
-            tma_load_2d_pair(sb + cch * 8192, mB, full_leader, bcol + cch * 64, brow, pol_b);
+          tma_load_3d_pair(sb, mB, full_leader, 0, brow, bcol / 64, pol_b);
           ++issued;
           if (++stage == kPairStages) {
             stage = 0;
@@ -354,7 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint16_t* crow = p.C + static_cast<size_t>(ctl.row0[g] + (valid ? row : 0)) * p.N + col0;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * 256;
       const int cols_per_part = hw / kEpiParts;
-      for (int cc = part * cols_per_part; cc < (part + 1) * cols_per_part; cc += kOutBoxCols) {
+      // a warp whose 32 rows all lie past the group's end has nothing to store
+      const int cc_end = warp_row0 < nrows_g ? (part + 1) * cols_per_part : 0;
+      for (int cc = part * cols_per_part; cc < cc_end; cc += kOutBoxCols) {
         if (col0 + cc >= p.N) break;  // box past the last column (half-empty last tile)
         uint32_t packed[16];
         if (kSwiGLU) {
@@ -456,6 +470,21 @@ cudaError_t make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t co
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         box_cols * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// 3-D bf16 tensor map of the weights [rows, cols] (cols % 64 == 0) viewed as
+// {64 columns, rows, cols / 64 column blocks}: a box {64, 64, nblk} holds nblk
+// consecutive 64-column blocks of 64 rows, each block 8 KB in shared memory
+// with the 128-byte swizzle; blocks past the last column read zeros.
+cudaError_t make_weight_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t nblk) {
+  cuuint64_t dims[3] = {64, rows, cols / 64};
+  cuuint64_t strides[2] = {cols * 2, 128};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBK), nblk};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -562,12 +591,12 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
   const int hw = 128;  // the last tile is half empty when F % 128 == 64
   CUtensorMap mA, mAs, mB0, mB1, mB0s, mB1s;
   if ((e = make_map(&mA, x_sorted, S, d.D, 128, kBK)) != cudaSuccess) return e;
-  if ((e = make_map(&mB0, W1, static_cast<uint64_t>(d.E) * d.D, d.F, kBK, 64)) != cudaSuccess) return e;
-  if ((e = make_map(&mB1, W3, static_cast<uint64_t>(d.E) * d.D, d.F, kBK, 64)) != cudaSuccess) return e;
+  if ((e = make_weight_map(&mB0, W1, static_cast<uint64_t>(d.E) * d.D, d.F, hw / 64)) != cudaSuccess) return e;
+  if ((e = make_weight_map(&mB1, W3, static_cast<uint64_t>(d.E) * d.D, d.F, hw / 64)) != cudaSuccess) return e;
   if (shared) {
     if ((e = make_map(&mAs, x, d.T, d.D, 128, kBK)) != cudaSuccess) return e;
-    if ((e = make_map(&mB0s, Ws1, d.D, d.F, kBK, 64)) != cudaSuccess) return e;
-    if ((e = make_map(&mB1s, Ws3, d.D, d.F, kBK, 64)) != cudaSuccess) return e;
+    if ((e = make_weight_map(&mB0s, Ws1, d.D, d.F, hw / 64)) != cudaSuccess) return e;
+    if ((e = make_weight_map(&mB1s, Ws3, d.D, d.F, hw / 64)) != cudaSuccess) return e;
   } else {
     mAs = mA;
     mB0s = mB0;
@@ -605,9 +634,9 @@ cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uin
   const uint64_t hrows = static_cast<uint64_t>(S) + (shared ? d.T : 0);
   CUtensorMap mA, mB0, mB0s;
   if ((e = make_map(&mA, h, hrows, d.F, 128, kBK)) != cudaSuccess) return e;
-  if ((e = make_map(&mB0, W2, static_cast<uint64_t>(d.E) * d.F, d.D, kBK, 64)) != cudaSuccess) return e;
+  if ((e = make_weight_map(&mB0, W2, static_cast<uint64_t>(d.E) * d.F, d.D, tn / 128)) != cudaSuccess) return e;
   if (shared) {
-    if ((e = make_map(&mB0s, Ws2, d.F, d.D, kBK, 64)) != cudaSuccess) return e;
+    if ((e = make_weight_map(&mB0s, Ws2, d.F, d.D, tn / 128)) != cudaSuccess) return e;
   } else {
     mB0s = mB0;
   }

@@ -185,6 +185,16 @@ MOE_DEV void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar
       : "memory");
 }
 
+// As tma_load_2d_pair for a 3-D tensor map (coordinates c0 = innermost, c1, c2).
+MOE_DEV void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                              int32_t c1, int32_t c2, uint64_t cache_policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(cache_policy)
+      : "memory");
+}
+
 // Stores the 2-D box at coordinates (c0, c1) from shared memory at `src`
 // (bulk async group of the executing thread).  c0 * element size must be a
 // multiple of 16 bytes and neither coordinate may be negative.
