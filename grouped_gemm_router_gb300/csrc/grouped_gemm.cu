@@ -572,6 +572,26 @@ cudaError_t tensor_map_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64
   return make_map(m, ptr, rows, cols, box_rows, box_cols);
 }
 
+cudaError_t tensor_map_f32_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                              uint32_t box0, uint32_t box1) {
+  {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
+  }
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 4, d0 * d1 * 4};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapSwizzle sw = box0 * 4 == 64    ? CU_TENSOR_MAP_SWIZZLE_64B
+                                : box0 * 4 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                  : CU_TENSOR_MAP_SWIZZLE_NONE;
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t device_error_address(unsigned int** p) {
   void* a = nullptr;
   cudaError_t e = cudaGetSymbolAddress(&a, g_device_error);

@@ -55,8 +55,14 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kOutBoxRows = 32;
 constexpr int kOutBoxCols = 32;
 constexpr int kOutBoxBytes = kOutBoxRows * kOutBoxCols * 2;
+constexpr int kWOutCols = 16;                 // fp32 weight-gradient store box: 32 rows x 64 bytes
 
 enum : int { kDgradW2 = 0, kActBwd = 1, kDgradX = 2, kWgrad = 3 };
+
+// Tensor maps per launch: A, A of the shared group, B0, B1, B0 / B1 of the
+// shared group, and five output maps (C, C2 in the row modes; the weight
+// gradient's w_a, w_b, ws_a, ws_b and partial slots).
+constexpr int kMaps = 11;
 
 // Weight-gradient tiles differ in length (a group's rows); up to kMaxLptTiles
 // of them are assigned longest first to the least-loaded pair.
@@ -157,7 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const __grid_constant__ CUtensorMap mapB0_sh,
                             const __grid_constant__ CUtensorMap mapB1_sh,
                             const __grid_constant__ CUtensorMap mapC,
-                            const __grid_constant__ CUtensorMap mapC2, const BwdArgs p) {
+                            const __grid_constant__ CUtensorMap mapC2,
+                            const __grid_constant__ CUtensorMap mapC3,
+                            const __grid_constant__ CUtensorMap mapC4,
+                            const __grid_constant__ CUtensorMap mapC5, const BwdArgs p) {
   using Tr = Traits<kMode>;
   constexpr int kSt = stages_of(kMode);
   extern __shared__ uint8_t bwd_smem_raw[];
@@ -355,6 +364,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
       my_count = mx <= kMaxMyTiles ? mine : -1;
+      // The same tiles round robin over the largest multiple P of the tiles
+      // per K chunk: every round then holds whole chunks, so the tiles that
+      // read the same rows run together and share them in L2 (a chunk split
+      // across rounds is read from DRAM twice).  Taken when its makespan is
+      // within 1/32 of the greedy one.
+      const int per_chunk = nmt * ntn;
+      const int P = per_chunk > 0 ? (npairs / per_chunk) * per_chunk : 0;
+      if (P > 0) {
+        uint32_t lpt_max = max(max(load[0], load[1]), max(load[2], load[3]));
+        uint32_t rr_max = 0;
+        for (int q = 0; q < 4; ++q) {
+          const int pid = lane + 32 * q;
+          if (pid >= P) continue;
+          uint32_t sum = 0;
+          int ps = 0;
+          for (int t = pid; t < total_t; t += P) {
+            while (t >= ctl.tile_prefix[ps + 1]) ++ps;
+            sum += static_cast<uint32_t>(chunk_kb_of(ctl.gorder[ps])) + 2u;
+          }
+          rr_max = max(rr_max, sum);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          lpt_max = max(lpt_max, __shfl_xor_sync(0xffffffffu, lpt_max, off));
+          rr_max = max(rr_max, __shfl_xor_sync(0xffffffffu, rr_max, off));
+        }
+        if (rr_max <= lpt_max + lpt_max / 32) my_count = -2;
+      }
     }
     if (lane == 0) ctl.my_count = my_count;
   }
@@ -367,9 +404,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &ctl.abort;
   unsigned int* dev_err = p.dev_err;
 
-  // the it-th tile of this pair (-1: none left)
+  // the it-th tile of this pair (-1: none left).  my_count: >= 0 tiles in
+  // my_tiles (greedy), -1 round robin over all pairs, -2 round robin over the
+  // largest multiple of the tiles per K chunk (whole chunks per round).
   const int my_n = ctl.my_count;
+  const int wg_pairs = my_n == -2 ? (npairs / (nmt * ntn)) * (nmt * ntn) : npairs;
   auto next_tile = [&](int it) -> int {
+    if (my_n == -2) {
+      const int t = pair + it * wg_pairs;
+      return pair < wg_pairs && t < total ? t : -1;
+    }
     if (my_n >= 0) return it < my_n ? ctl.my_tiles[it] : -1;
     const int t = pair + it * npairs;
     return t < total ? t : -1;
@@ -671,36 +715,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // kWgrad: fp32 rows m * 256 + r (< M), columns n * 256 + cc (< N);
-        // a split group's chunk goes to its partial slot
+        // a split group's chunk goes to its partial slot.  Each 32 x 16 box
+        // is staged with the 64-byte swizzle (conflict-free 16-byte writes)
+        // and written by one TMA store; rows past M are clipped by the map.
         const bool empty_k = ti.kb1 <= ti.kb0;
         const bool split = ctl.nchunk[g] > 1;
-        const int row = m * kTileM + r_in_tile;
-        const bool valid = row < p.M;
+        const int warp_row0 = m * kTileM + 128 * static_cast<int>(rank) + q * 32;
+        const bool any_row = warp_row0 < p.M;
         for (int cc = part * cols_per_part; cc < (part + 1) * cols_per_part; cc += 32) {
           const int col = n * kTileN + cc;
-          if (col >= p.N) break;
+          if (col >= p.N || !any_row) break;
           uint32_t ra[32];
           tmem_ld_32cols(taddr + cc, ra);
           tmem_ld_wait();
-          if (!valid) continue;
-          float* dst;
+          const CUtensorMap* om;
+          int x, z;
           if (split) {
-            dst = p.part + (static_cast<size_t>(ctl.pslot[g] + ti.c) * p.M + row) * p.N + col;
+            om = &mapC5;
+            x = col;
+            z = ctl.pslot[g] + ti.c;
           } else {
             const bool second = col >= p.n_split;
-            float* base = routed ? (second ? p.w_b : p.w_a) : (second ? p.ws_b : p.ws_a);
-            const int ncols = second ? p.N - p.n_split : p.n_split;
-            const int c0 = second ? col - p.n_split : col;
-            dst = base + (routed ? static_cast<size_t>(g) * p.M * ncols : 0) + static_cast<size_t>(row) * ncols + c0;
+            om = routed ? (second ? &mapC2 : &mapC) : (second ? &mapC4 : &mapC3);
+            x = second ? col - p.n_split : col;
+            z = routed ? g : 0;
           }
-          float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            if (empty_k)
-              d4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-            else
-              d4[v] = make_float4(__uint_as_float(ra[4 * v]), __uint_as_float(ra[4 * v + 1]),
-                                  __uint_as_float(ra[4 * v + 2]), __uint_as_float(ra[4 * v + 3]));
+          for (int hh = 0; hh < 2; ++hh) {
+            bulk_wait_group_read0();  // the previous box's store has read the buffer
+            __syncwarp();
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int j = 16 * hh + 4 * v;
+              const uint4 val = empty_k ? make_uint4(0u, 0u, 0u, 0u)
+                                        : make_uint4(ra[j], ra[j + 1], ra[j + 2], ra[j + 3]);
+              *reinterpret_cast<uint4*>(stage_out + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = val;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(om, smem_u32(stage_out), x + kWOutCols * hh, warp_row0, z);
+              bulk_commit_group();
+            }
           }
         }
       }
@@ -815,7 +871,7 @@ cudaError_t bwd_setup(BwdDevice* out) {
 }
 
 template <int kMode>
-cudaError_t launch_mode(const CUtensorMap (&m)[8], BwdArgs a, cudaStream_t s, bool pdl) {
+cudaError_t launch_mode(const CUtensorMap (&m)[kMaps], BwdArgs a, cudaStream_t s, bool pdl) {
   BwdDevice bd;
   cudaError_t e = bwd_setup(&bd);
   if (e != cudaSuccess) return e;
@@ -835,7 +891,7 @@ cudaError_t launch_mode(const CUtensorMap (&m)[8], BwdArgs a, cudaStream_t s, bo
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, grouped_gemm_bwd_kernel<kMode>, m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7],
-                         a);
+                         m[8], m[9], m[10], a);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -866,7 +922,7 @@ cudaError_t launch_bwd_dgrad_w2(const BwdLayout& L, const int32_t* offsets, cons
                                 uint16_t* hbar, cudaStream_t s, bool pdl) {
   const moe_dims& d = L.d;
   const uint64_t rows = static_cast<uint64_t>(L.S_pad) + (L.shared ? d.T : 0);
-  CUtensorMap m[8];
+  CUtensorMap m[kMaps];
   cudaError_t e;
   if ((e = tensor_map_2d(&m[0], ybar, L.S_pad, d.D, 128, kBK)) != cudaSuccess) return e;
   if ((e = tensor_map_2d(&m[2], W2, static_cast<uint64_t>(d.E) * d.F, d.D, 128, kBK)) != cudaSuccess) return e;
@@ -886,6 +942,7 @@ cudaError_t launch_bwd_dgrad_w2(const BwdLayout& L, const int32_t* offsets, cons
   a.b_rows = d.F;
   a.C = hbar;
   m[7] = m[6];
+  m[8] = m[9] = m[10] = m[6];
   return launch_mode<kDgradW2>(m, a, s, pdl);
 }
 
@@ -895,7 +952,7 @@ cudaError_t launch_bwd_act(const BwdLayout& L, const int32_t* offsets, const uin
                            uint16_t* gu, uint16_t* h, cudaStream_t s, bool pdl) {
   const moe_dims& d = L.d;
   const int S = d.T * d.k;
-  CUtensorMap m[8];
+  CUtensorMap m[kMaps];
   cudaError_t e;
   if ((e = tensor_map_2d(&m[0], x_sorted, S, d.D, 128, kBK)) != cudaSuccess) return e;
   if ((e = tensor_map_2d(&m[2], W1, static_cast<uint64_t>(d.E) * d.D, d.F, kBK, 64)) != cudaSuccess) return e;
@@ -922,6 +979,7 @@ cudaError_t launch_bwd_act(const BwdLayout& L, const int32_t* offsets, const uin
   a.hbar = hbar;
   a.gu = gu;
   a.h = h;
+  m[8] = m[9] = m[10] = m[6];
   return launch_mode<kActBwd>(m, a, s, pdl);
 }
 
@@ -930,7 +988,7 @@ cudaError_t launch_bwd_dgrad_x(const BwdLayout& L, const int32_t* offsets, const
                                const uint16_t* Ws3, uint16_t* xbar, cudaStream_t s, bool pdl) {
   const moe_dims& d = L.d;
   const uint64_t rows = static_cast<uint64_t>(L.S_pad) + (L.shared ? d.T : 0);
-  CUtensorMap m[8];
+  CUtensorMap m[kMaps];
   cudaError_t e;
   if ((e = tensor_map_2d(&m[0], gu, L.S_pad, 2 * d.F, 128, kBK)) != cudaSuccess) return e;
   if ((e = tensor_map_2d(&m[2], W1, static_cast<uint64_t>(d.E) * d.D, d.F, 128, kBK)) != cudaSuccess) return e;
@@ -953,6 +1011,7 @@ cudaError_t launch_bwd_dgrad_x(const BwdLayout& L, const int32_t* offsets, const
   a.b_rows = d.D;
   a.C = xbar;
   m[7] = m[6];
+  m[8] = m[9] = m[10] = m[6];
   return launch_mode<kDgradX>(m, a, s, pdl);
 }
 
@@ -962,7 +1021,7 @@ cudaError_t launch_bwd_wgrad(const BwdLayout& L, const int32_t* offsets, const u
                              float* ws_b, float* part, cudaStream_t s, bool pdl) {
   const moe_dims& d = L.d;
   const int S = d.T * d.k;
-  CUtensorMap m[8];
+  CUtensorMap m[kMaps];
   cudaError_t e;
   if ((e = tensor_map_2d(&m[0], A, a_padded ? L.S_pad : S, M, kBK, 64)) != cudaSuccess) return e;
   if ((e = tensor_map_2d(&m[2], B, L.S_pad, N, kBK, 64)) != cudaSuccess) return e;
@@ -975,7 +1034,28 @@ cudaError_t launch_bwd_wgrad(const BwdLayout& L, const int32_t* offsets, const u
   }
   m[3] = m[2];
   m[5] = m[4];
-  m[6] = m[0];
+  // fp32 outputs as {columns, M, group or slot}: 16 x 32 boxes, rows past M clipped
+  const int nb = N - n_split;
+  const uint64_t slots = bwd_wgrad_part_floats(d, L.shared) / (2 * static_cast<uint64_t>(d.D) * d.F);
+  if ((e = tensor_map_f32_3d(&m[6], w_a, n_split, M, d.E, kWOutCols, kOutBoxRows)) != cudaSuccess) return e;
+  // nb == 0 (one output, no second half): its maps are never used
+  if (nb > 0) {
+    if ((e = tensor_map_f32_3d(&m[7], w_b, nb, M, d.E, kWOutCols, kOutBoxRows)) != cudaSuccess) return e;
+  } else {
+    m[7] = m[6];
+  }
+  if (L.shared) {
+    if ((e = tensor_map_f32_3d(&m[8], ws_a, n_split, M, 1, kWOutCols, kOutBoxRows)) != cudaSuccess) return e;
+    if (nb > 0) {
+      if ((e = tensor_map_f32_3d(&m[9], ws_b, nb, M, 1, kWOutCols, kOutBoxRows)) != cudaSuccess) return e;
+    } else {
+      m[9] = m[8];
+    }
+  } else {
+    m[8] = m[6];
+    m[9] = m[7];
+  }
+  if ((e = tensor_map_f32_3d(&m[10], part, N, M, slots, kWOutCols, kOutBoxRows)) != cudaSuccess) return e;
   BwdArgs a = base_args(L, offsets);
   a.M = M;
   a.N = N;
@@ -986,7 +1066,6 @@ cudaError_t launch_bwd_wgrad(const BwdLayout& L, const int32_t* offsets, const u
   a.ws_a = ws_a;
   a.ws_b = ws_b;
   a.part = part;
-  m[7] = m[6];
   e = launch_mode<kWgrad>(m, a, s, pdl);
   if (e != cudaSuccess) return e;
   const size_t mn4 = (static_cast<size_t>(M) * N / 4 + 255) / 256;

@@ -205,6 +205,14 @@ MOE_DEV void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0, int3
                : "memory");
 }
 
+// As tma_store_2d for a 3-D tensor map; elements outside the tensor are not written.
+MOE_DEV void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1, int32_t c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(src)
+               : "memory");
+}
+
 MOE_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Waits until no bulk group of this thread still reads shared memory.

@@ -129,6 +129,10 @@ cudaError_t launch_router_bwd(const BwdLayout& L, const uint16_t* x_sorted, cons
 // zero fill outside the tensor (grouped_gemm.cu).
 cudaError_t tensor_map_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
                           uint32_t box_rows, uint32_t box_cols);
+// 3-D fp32 TMA descriptor of a packed [d2][d1][d0] array with a {box0, box1, 1}
+// box: 64-byte swizzle for 16-float boxes (128-byte for 32), none otherwise.
+cudaError_t tensor_map_f32_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                              uint32_t box0, uint32_t box1);
 
 // Device address of the error word that moe_device_error reads, on the
 // current device.
