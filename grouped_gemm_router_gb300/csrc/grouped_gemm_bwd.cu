@@ -619,6 +619,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool full_box = warp_row0 + kOutBoxRows <= nvalid;
         const int col0 = n * hw;
         constexpr int kChunks = (kMode == kActBwd ? kTileN / 2 : kTileN) / 2 / kOutBoxCols;
+        // The plain-output modes read all of this warp's accumulator columns
+        // in one burst with a single wait and hand the accumulator back
+        // before packing and storing (a wait after every 32-column box holds
+        // the MMAs back).  The SwiGLU-backward mode keeps its h_bar rows in
+        // registers too and reads its two g|u boxes one at a time.
+        uint32_t acc[kMode == kActBwd ? 1 : kChunks][32];
+        if (kMode != kActBwd) {
+#pragma unroll
+          for (int c2 = 0; c2 < kChunks; ++c2) tmem_ld_32cols(taddr + part * cols_per_part + c2 * kOutBoxCols, acc[c2]);
+          tmem_ld_wait();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
+        }
 #pragma unroll
         for (int c2 = 0; c2 < kChunks; ++c2) {
           const int cc = part * cols_per_part + c2 * kOutBoxCols;
@@ -687,13 +701,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           } else {
-            uint32_t ra[32];
-            tmem_ld_32cols(taddr + cc, ra);
-            tmem_ld_wait();
             uint32_t packed[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              packed[j] = pack_bf16x2(__uint_as_float(ra[2 * j]), __uint_as_float(ra[2 * j + 1]));
+              packed[j] = pack_bf16x2(__uint_as_float(acc[c2][2 * j]), __uint_as_float(acc[c2][2 * j + 1]));
             if (full_box) {
               bulk_wait_group_read0();
               __syncwarp();
@@ -722,12 +733,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool split = ctl.nchunk[g] > 1;
         const int warp_row0 = m * kTileM + 128 * static_cast<int>(rank) + q * 32;
         const bool any_row = warp_row0 < p.M;
-        for (int cc = part * cols_per_part; cc < (part + 1) * cols_per_part; cc += 32) {
+        // all of this warp's columns in one burst, then the accumulator is released
+        constexpr int kBoxes = kTileN / 2 / 32;
+        uint32_t acc[kBoxes][32];
+        if (any_row) {
+#pragma unroll
+          for (int b = 0; b < kBoxes; ++b) tmem_ld_32cols(taddr + part * cols_per_part + 32 * b, acc[b]);
+          tmem_ld_wait();
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
+#pragma unroll
+        for (int b = 0; b < kBoxes; ++b) {
+          const int cc = part * cols_per_part + 32 * b;
           const int col = n * kTileN + cc;
           if (col >= p.N || !any_row) break;
-          uint32_t ra[32];
-          tmem_ld_32cols(taddr + cc, ra);
-          tmem_ld_wait();
+          const uint32_t(&ra)[32] = acc[b];
           const CUtensorMap* om;
           int x, z;
           if (split) {
@@ -760,9 +782,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
+      if (kMode == kActBwd) {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
+      }
     }
     if (lane == 0) bulk_wait_group0();
     __syncwarp();
