@@ -285,27 +285,75 @@ __global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ i
 //     (offsets[e] + the counts of expert e in blocks before b).
 //  2. Slots are ranked stably in rounds of 256 (one per thread): within a
 //     warp by __match_any_sync, across warps by per-warp counts.
-//  3. perm/inv are written and x rows are copied to x_sorted with 16-byte
-//     vector loads and stores, one warp per row.
+//  3. perm/inv are written and the x rows are copied to x_sorted by bulk
+//     copies: the block's rows stream into two shared-memory buffers (one
+//     1-D bulk load per chunk of rows, issued before the wait on the router,
+//     since x does not come from it), and each of a row's k copies leaves
+//     by one bulk store to its sorted position.
 constexpr int kScatterThreads = 256;
 constexpr int kScatterWarps = kScatterThreads / 32;
+constexpr int kScatterBufBytes = 16384;  // one of the two row staging buffers
+
+// 1-D bulk copy of `bytes` (a multiple of 16) from global memory into shared
+// memory, counted on the transaction barrier `bar`.
+MOE_DEV void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// 1-D bulk copy of `bytes` (a multiple of 16) from shared to global memory,
+// in the bulk async group of the executing thread.
+MOE_DEV void bulk_store_1d(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
 
 __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
     const int32_t* __restrict__ ids, const int32_t* __restrict__ hist, int T, int k, int E, int TB,
     int nblk,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
-    int32_t* __restrict__ inv, const uint4* __restrict__ x, uint4* __restrict__ xs, int D) {
+    int32_t* __restrict__ inv, const uint16_t* __restrict__ x, uint16_t* __restrict__ xs, int D,
+    unsigned int* dev_err) {
+  extern __shared__ __align__(128) uint8_t sc_stage[];  // 2 x kScatterBufBytes when x is copied
+  __shared__ uint64_t sc_full[2];
+  __shared__ int sc_abort;
   __shared__ int s_red_pre[kScatterThreads];
   __shared__ int s_red_tot[kScatterThreads];
   __shared__ int s_base[MOE_MAX_EXPERTS];
   __shared__ int s_wcnt[kScatterWarps][MOE_MAX_EXPERTS];
   __shared__ int s_pos[64 * MOE_MAX_TOPK];
 
-  griddep_wait();  // ids and the block histogram come from the previous kernel
-  griddep_launch_dependents();
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = T * k;
+
+  // ---- 0. start streaming this block's x rows (chunks of RB rows) ----
+  const int t0 = b * TB;
+  const int ntok = min(TB, T - t0);
+  const uint32_t rowb = static_cast<uint32_t>(D) * 2u;
+  const int RB = max(1, kScatterBufBytes / static_cast<int>(rowb));
+  const int nch = (x != nullptr && xs != nullptr) ? (ntok + RB - 1) / RB : 0;
+  auto load_chunk = [&](int c) {  // one thread
+    const int r0 = c * RB, nr = min(RB, ntok - r0);
+    const uint32_t bar = smem_u32(&sc_full[c & 1]);
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr) * rowb);
+    bulk_load_1d(smem_u32(sc_stage + (c & 1) * kScatterBufBytes), x + static_cast<size_t>(t0 + r0) * D,
+                 static_cast<uint32_t>(nr) * rowb, bar);
+  };
+  if (tid == 0) {
+    sc_abort = 0;
+    if (nch > 0) {
+      mbar_init(smem_u32(&sc_full[0]), 1);
+      mbar_init(smem_u32(&sc_full[1]), 1);
+      fence_mbar_init();
+      fence_proxy_async_smem();
+      load_chunk(0);
+      if (nch > 1) load_chunk(1);
+    }
+  }
+  griddep_wait();  // ids and the block histogram come from the previous kernel
+  griddep_launch_dependents();
 
   // ---- 1. column sums of the block histogram ----
   {
@@ -397,38 +445,35 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
     __syncthreads();
   }
 
-  // ---- 3. gather rows: each warp copies 4 rows at a time ----
-  if (x == nullptr) return;
-  const int n16 = D >> 3;  // 16-byte vectors per row
-  constexpr int RW = 4;
-  for (int i0 = warp * RW; i0 < ns; i0 += kScatterWarps * RW) {
-    const uint4* src[RW];
-    uint4* dst[RW];
-#pragma unroll
-    for (int r = 0; r < RW; ++r) {
-      const int i = i0 + r;
-      const bool ok = i < ns && s_pos[i] >= 0;
-      src[r] = ok ? x + static_cast<size_t>((s0 + i) / k) * n16 : nullptr;
-      dst[r] = ok ? xs + static_cast<size_t>(s_pos[i]) * n16 : nullptr;
+  // ---- 3. copy rows: chunk c sits in buffer c % 2; its k copies per row
+  // are bulk stores issued one per thread, and the buffer is refilled with
+  // chunk c + 2 once every store has read it ----
+  if (nch == 0) return;
+  int c = 0;
+  for (; c < nch; ++c) {
+    const int r0 = c * RB, nr = min(RB, ntok - r0);
+    const bool ok = mbar_wait(smem_u32(&sc_full[c & 1]), (c >> 1) & 1, &sc_abort, dev_err);
+    if (!__syncthreads_and(ok)) break;
+    const uint32_t sbuf = smem_u32(sc_stage + (c & 1) * kScatterBufBytes);
+    for (int i = tid; i < nr * k; i += kScatterThreads) {
+      const int pos = s_pos[r0 * k + i];
+      if (pos >= 0) bulk_store_1d(xs + static_cast<size_t>(pos) * D, sbuf + (i / k) * rowb, rowb);
     }
-    for (int c0 = lane; c0 < n16; c0 += 64) {
-      uint4 v[RW][2];
-#pragma unroll
-      for (int r = 0; r < RW; ++r)
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int cidx = c0 + 32 * u;
-          if (src[r] != nullptr && cidx < n16) v[r][u] = __ldg(src[r] + cidx);
-        }
-#pragma unroll
-      for (int r = 0; r < RW; ++r)
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int cidx = c0 + 32 * u;
-          if (dst[r] != nullptr && cidx < n16) dst[r][cidx] = v[r][u];
-        }
+    bulk_commit_group();
+    if (c + 2 < nch) {
+      bulk_wait_group_read0();  // this thread's stores have read the buffer
+      __syncthreads();
+      if (tid == 0) load_chunk(c + 2);
     }
   }
+  if (c < nch && tid == 0) {
+    // A wait gave up: let the loads still in flight land before the block
+    // exits (bounded as well; the error word is already set).
+    volatile int local_abort = 0;
+    for (int cc = c; cc < nch && cc < c + 2; ++cc)
+      mbar_wait(smem_u32(&sc_full[cc & 1]), (cc >> 1) & 1, &local_abort, dev_err);
+  }
+  bulk_wait_group0();
 }
 
 template <int NT, int KMAX>
@@ -489,13 +534,30 @@ cudaError_t launch_hist(const int32_t* ids, const moe_dims& d, int32_t* hist, cu
                        route_block_tokens(d.T), hist);
 }
 
+// Device error word of the current device (cached per device).
+static cudaError_t scatter_error_word(unsigned int** out) {
+  static unsigned int* words[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (words[dev] == nullptr && (e = device_error_address(&words[dev])) != cudaSuccess) return e;
+  *out = words[dev];
+  return cudaSuccess;
+}
+
 cudaError_t launch_scatter(const int32_t* ids, const int32_t* hist, const moe_dims& d, int32_t* counts,
                            int32_t* offsets, int32_t* perm, int32_t* inv, const uint16_t* x,
                            uint16_t* x_sorted, cudaStream_t s, bool pdl) {
   const int nblk = route_blocks(d.T);
-  return launch_kernel(scatter_kernel, dim3(nblk), dim3(kScatterThreads), 0, s, pdl, ids, hist, d.T, d.k, d.E,
-                       route_block_tokens(d.T), nblk, counts, offsets, perm, inv,
-                       reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(x_sorted), d.D);
+  unsigned int* dev_err = nullptr;
+  cudaError_t e = scatter_error_word(&dev_err);
+  if (e != cudaSuccess) return e;
+  const size_t smem = (x != nullptr && x_sorted != nullptr) ? 2 * kScatterBufBytes : 0;
+  return launch_kernel(scatter_kernel, dim3(nblk), dim3(kScatterThreads), smem, s, pdl, ids, hist, d.T, d.k,
+                       d.E, route_block_tokens(d.T), nblk, counts, offsets, perm, inv, x, x_sorted, d.D, dev_err);
 }
 
 }  // namespace moe
