@@ -29,7 +29,11 @@ MOE_DEV void fma_bf16x8(float (&acc)[8], float w, const uint4& v) {
 
 // One warp per token.  KMAX >= k is a compile-time bound so the k row
 // pointers and weights stay in registers; each lane loads all k (+1) rows of
-// U 16-byte column chunks before doing any arithmetic.
+// U 16-byte column chunks before doing any arithmetic.  Every y row is read
+// once and every out row written once, so both go through L2 with the
+// evict-first (streaming) policy: the L2 is full of the grouped GEMM's dirty
+// y lines when this kernel starts, and the streamed lines should be the
+// first to leave.
 template <int KMAX, int U>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const uint4* __restrict__ y, const float* __restrict__ w, const int32_t* __restrict__ inv, int T,
@@ -64,8 +68,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
       const bool in = c < n16;
 #pragma unroll
       for (int j = 0; j < KMAX; ++j)
-        if (j < k && in) v[u][j] = __ldg(rows[j] + c);
-      vs[u] = (has_shared && in) ? __ldg(ysh + c) : make_uint4(0, 0, 0, 0);
+        if (j < k && in) v[u][j] = __ldcs(rows[j] + c);
+      vs[u] = (has_shared && in) ? __ldcs(ysh + c) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -90,7 +94,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
       o.y = pack_bf16x2(acc[2], acc[3]);
       o.z = pack_bf16x2(acc[4], acc[5]);
       o.w = pack_bf16x2(acc[6], acc[7]);
-      orow[c] = o;
+      __stcs(orow + c, o);
     }
   }
 }
