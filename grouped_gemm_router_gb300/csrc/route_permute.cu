@@ -361,10 +361,19 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
     const int e = tid % E, r = tid / E;
     int pre = 0, tot = 0;
     if (r < R) {
-      for (int bb = r; bb < nblk; bb += R) {
-        const int hv = hist[static_cast<size_t>(bb) * E + e];
-        tot += hv;
-        if (bb < b) pre += hv;
+      // eight independent loads in flight per batch (these L2 reads are latency-bound)
+      for (int bb0 = r; bb0 < nblk; bb0 += 8 * R) {
+        int hv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int bb = bb0 + u * R;
+          hv[u] = bb < nblk ? hist[static_cast<size_t>(bb) * E + e] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          tot += hv[u];
+          if (bb0 + u * R < b) pre += hv[u];
+        }
       }
     }
     s_red_pre[tid] = pre;
