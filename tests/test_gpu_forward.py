@@ -214,3 +214,21 @@ def test_forward_and_backward_replay_from_a_cuda_graph(moe):
     assert torch.equal(out, eager_out)
     for name in eager_g:
         assert torch.equal(graph_g[name], eager_g[name]), name
+
+
+def test_forward_at_the_dimension_cap(moe):
+    """D = F = 8192 (the library's cap): 128 k-blocks per W1||W3 tile, 64 column
+    tiles, one 16 KB row per scatter staging buffer.  Ragged T, shared expert;
+    sampled tokens against the oracle."""
+    T, D, F, E, k = 80, 8192, 8192, 2, 2
+    w_, L = inputs.make_custom(T, D, F, E, k, True, 41)
+    G = _dev_layer(L)
+    out = moe.moe_ffn_forward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], k, Ws1=G["Ws1"], Ws3=G["Ws3"],
+                              Ws2=G["Ws2"])
+    torch.cuda.synchronize()
+    assert moe.device_error() == 0
+    tokens = np.array([0, 1, 37, 63, 64, 79])
+    logits = orc.router_logits(orc.bf16_to_f64(L["x"][tokens]), orc.bf16_to_f64(L["Wg"]))
+    assert (orc.topk_gap(logits, k) >= 1e-3).all()   # k = E: every expert, no near tie
+    ref = _oracle(L, k, tokens)
+    assert_close(to_f64(out)[tokens], ref["out"], "out at D = F = 8192")
