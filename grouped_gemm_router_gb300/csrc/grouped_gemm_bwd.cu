@@ -608,6 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool got = mbar_wait_cluster(smem_u32(&ctl.tfull[buf]), tph, abort_flag, dev_err);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
+      bool act_released = false;  // kActBwd: accumulator already handed back
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * 256;
       const int cols_per_part = hw / 2;
       if (Tr::row_tiles) {
@@ -642,6 +643,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_32cols(taddr + cc, rg);
             tmem_ld_32cols(taddr + hw + cc, ru);
             tmem_ld_wait();
+            if (c2 == kChunks - 1 || col0 + cc + kOutBoxCols >= p.N) {
+              // the last box is in registers: hand the accumulator back
+              // before its math and stores
+              tc_fence_before_sync();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
+              act_released = true;
+            }
             const uint32_t(&hb)[16] = hbp[c2 < 2 ? c2 : 1];
             if (full_box) {
               bulk_wait_group_read0();  // the previous chunk's stores have read the buffers
@@ -782,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (kMode == kActBwd) {
+      if (kMode == kActBwd && !act_released) {
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
