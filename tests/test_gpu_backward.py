@@ -208,11 +208,13 @@ def test_backward_fixed_routing_skips_router(moe):
         assert_wgrad(to_f64(g[n]), ref[n], n)
 
 
-@pytest.mark.parametrize("name", ["gptoss_lite"])
+@pytest.mark.parametrize("name", ["gptoss_lite", "skewed", "small_chunk"])
 def test_backward_full_size_sampled(moe, name):
-    """The benchmark's workload with routing fixed from outside: dx on sampled
+    """Full-size workloads with routing fixed from outside: dx on sampled
     tokens and sampled columns of every weight gradient, each computed by the
-    oracle from the rows it needs."""
+    oracle from the rows it needs.  skewed adds Zipf load, an empty expert
+    (whose gradients must be exactly zero) and groups split along their rows;
+    small_chunk adds 64 experts of ~128 rows, top-4 and the shared expert."""
     w_ = inputs.WORKLOADS[name]
     L = inputs.make_layer(w_)
     T, D, F, E, k = w_.T, w_.D, w_.F, w_.E, w_.k
@@ -239,7 +241,10 @@ def test_backward_full_size_sampled(moe, name):
         dx_ref += bwd.expert_backward(x64[tokens], Ws1, Ws3, Ws2, dout64[tokens])["xs_bar"]
     assert_dx(to_f64(g["dx"])[tokens], dx_ref, "dx sampled tokens")
     # sampled columns f of dW1[e], dW3[e] and rows f of dW2[e], from the expert's rows
-    for e in rng.choice(E, 3, replace=False):
+    experts = rng.choice(E, 3, replace=False)
+    if w_.empty_expert is not None:
+        experts = np.unique(np.append(experts, w_.empty_expert))
+    for e in experts:
         a, b = int(off[e]), int(off[e + 1])
         xs = x64[perm[a:b] // k]
         ybar = w[perm[a:b] // k, perm[a:b] % k][:, None] * dout64[perm[a:b] // k]
