@@ -208,7 +208,7 @@ def test_backward_fixed_routing_skips_router(moe):
         assert_wgrad(to_f64(g[n]), ref[n], n)
 
 
-@pytest.mark.parametrize("name", ["gptoss_lite", "skewed", "small_chunk"])
+@pytest.mark.parametrize("name", ["gptoss_lite", "skewed", "small_chunk", "wide"])
 def test_backward_full_size_sampled(moe, name):
     """Full-size workloads with routing fixed from outside: dx on sampled
     tokens and sampled columns of every weight gradient, each computed by the
