@@ -264,11 +264,97 @@ def test_w1w3_flop_count_matches_page():
     assert round(flops / 1e9) == g["gflop_printed"]
 
 
-def test_active_flops_decomposition():
-    # router + 3 routed GEMMs + 3 shared GEMMs, each 2 FLOPs per multiply-add
-    T, D, F, E, k = 32768, 768, 1536, 8, 2
-    assert orc.active_flops(T, D, F, E, k, True) == (
-        2 * T * D * E + orc.w1w3_flops(T, D, F, k) * 3 // 2 + 6 * T * D * F)
+class _MacCounter:
+    """Plain-Python evaluation of the layer that counts every multiply-add it
+    performs.  Only the experts a token is routed to are evaluated (the
+    'active' work), unlike the dense masked brute force above; the output is
+    returned so that the counted evaluation can be checked for correctness."""
+
+    def __init__(self):
+        self.macs = 0
+
+    def dot(self, a, b):
+        self.macs += len(a)
+        return sum(p * q for p, q in zip(a, b))
+
+    def vecmat(self, v, M):                # v [n] @ M [n][m]
+        return [self.dot(v, [M[i][j] for i in range(len(M))]) for j in range(len(M[0]))]
+
+    def swiglu(self, xrow, W1, W3, W2):
+        g, u = self.vecmat(xrow, W1), self.vecmat(xrow, W3)
+        h = [gi / (1.0 + math.exp(-gi)) * ui for gi, ui in zip(g, u)]
+        return self.vecmat(h, W2)
+
+    def layer(self, x, Wg, W1, W3, W2, k, Ws1=None, Ws3=None, Ws2=None):
+        x, Wg, W1, W3, W2 = map(_to_py, (x, Wg, W1, W3, W2))
+        out = []
+        for t in range(len(x)):
+            logits = self.vecmat(x[t], Wg)
+            chosen = sorted(range(len(W1)), key=lambda e: (-logits[e], e))[:k]
+            z = [math.exp(logits[e] - logits[chosen[0]]) for e in chosen]
+            acc = [0.0] * len(x[t])
+            for e, ze in zip(chosen, z):
+                y = self.swiglu(x[t], W1[e], W3[e], W2[e])
+                acc = [a + ze / sum(z) * yi for a, yi in zip(acc, y)]
+            if Ws1 is not None:
+                ys = self.swiglu(x[t], *map(_to_py, (Ws1, Ws3, Ws2)))
+                acc = [a + yi for a, yi in zip(acc, ys)]
+            out.append(acc)
+        return np.array(out)
+
+
+@pytest.mark.parametrize("T,D,F,E,k,shared", [(6, 8, 12, 5, 2, True), (5, 16, 8, 7, 3, False),
+                                              (4, 8, 8, 3, 3, True)])
+def test_active_flops_equals_counted_multiply_adds(T, D, F, E, k, shared):
+    """active_flops = 2 x the multiply-adds a sparse evaluation of the layer
+    actually performs (router, the k routed experts per token, the shared
+    expert).  A wrong router, routed or shared term changes the count."""
+    w_, L = _tiny(T, D, F, E, k, shared, seed=71 + T)
+    mc = _MacCounter()
+    got = mc.layer(L["x"], L["Wg"], L["W1"], L["W3"], L["W2"], k, L["Ws1"], L["Ws3"], L["Ws2"])
+    ref = _run_oracle(w_, L)["out"]
+    assert np.abs(got - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())   # the counted run is the layer
+    assert orc.active_flops(T, D, F, E, k, shared) == 2 * mc.macs
+    # the routed W1 and W3 products alone are the page's W1/W3 stage count
+    mc13 = _MacCounter()
+    xs, W1s, W3s = _to_py(L["x"]), _to_py(L["W1"]), _to_py(L["W3"])
+    for t in range(T):
+        for e in range(k):                     # any k experts: the count does not depend on which
+            mc13.vecmat(xs[t], W1s[e])
+            mc13.vecmat(xs[t], W3s[e])
+    assert orc.w1w3_flops(T, D, F, k) == 2 * mc13.macs
+
+
+def test_activation_traffic_saving_matches_page(monkeypatch):
+    """Part A section 6.2 of the Triton-MoE page: fusing W1/W3 with silu*mul
+    removes four activation streams (write g, write u, read g, read u) of
+    bf16 [slots, d_ff] tensors, 96 MiB for 4096 tokens x top-2 at d_ff = 1536.
+    The element counts are taken from the oracle's own g and u intermediates
+    at that shape (d_model does not enter them, so a small one is used)."""
+    g = json.load(open(os.path.join(GOLDEN, "p1_activation_traffic.json")))
+    T, k, E, F, D = g["slots"] // 2, 2, 8, g["d_ff"], 8
+    assert T * k == g["slots"]
+    rng = np.random.default_rng(0)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    pm = orc.permutation(ids, E)
+    x = rng.standard_normal((T, D))
+    xs = orc.gather_sorted(x, pm["perm"], k)
+    W1, W3 = rng.standard_normal((E, D, F)), rng.standard_normal((E, D, F))
+    seen = []
+    real_silu = orc.silu
+
+    def recording_silu(z):             # silu is applied to g, one expert's [rows, F] block at a time
+        seen.append(z.size)
+        return real_silu(z)
+    monkeypatch.setattr(orc, "silu", recording_silu)
+    h = orc.grouped_swiglu(xs, W1, W3, pm["offsets"])
+    g_elems = sum(seen)
+    u_elems = h.size                   # u has the shape of h (and of g)
+    assert g_elems == u_elems == g["slots"] * g["d_ff"]
+    streams = 2 * g_elems + 2 * u_elems          # write g, write u, read g, read u
+    saved = streams * g["bytes_per_element"]
+    assert g["streams_removed"] == 4
+    assert saved == g["mib_printed"] * 2 ** 20
 
 
 # ----------------------------------------------------------------------------
