@@ -4,7 +4,10 @@ A step is one forward pass of the whole layer (router -> top-k/softmax ->
 stable permutation -> W1||W3 + SiLU*mul -> W2 -> weighted combine, plus the
 shared expert) over one batch of synthetic tokens of the GPT-OSS-Lite-shaped
 workload (T=32768, D=768, F=1536, E=8 routed top-2 + 1 shared expert), with
-all inputs resident in HBM.  One JSON line is printed by rank 0.
+all inputs resident in HBM.  One JSON line is printed by rank 0.  On one GPU
+the line also carries `per_workload`: the same measurement (tokens/s, active
+TFLOP/s, roofline placement, stage times, clocks) for each of the other
+synthetic workloads (tiny, skewed, small_chunk, wide), with the same steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 
@@ -16,9 +19,10 @@ Multi-GPU (torchrun): every rank runs its own replica of the layer on its own
 batch (weak scaling, no collective on the data path); the step time is the max
 over ranks.
 
---impl reference times the fp64 CPU oracle as it stands on the host cores,
-on a bounded sample of the same workload, and prints the same line with
-"impl": "reference".
+--impl reference times the fp64 CPU oracle as it stands on the host cores
+(rank 0 only), every step on the first n tokens of the same workload with n
+sized so the run takes about a minute and a half, and prints the same line
+with "impl": "reference" and the time of the steps it actually ran.
 """
 from __future__ import annotations
 
@@ -42,6 +46,7 @@ WORKLOAD = "gptoss_lite"
 DATASHEET_BF16_DENSE_TFLOPS = 2250.0  # GB300 dense bf16 (the datasheet's sparse figure halved)
 METRIC = "MoE FFN fwd tokens/s and active TFLOP/s on 1 GB300; % of bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+REF_BUDGET_S = 90.0  # wall time of the reference arm's warm-up + timed steps
 
 
 def peaks():
@@ -212,32 +217,60 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def run_reference(args, w, rank):
+L2_NOTE = "flushed between steps (512 MB write + read back)"
+
+
+def line_config(w, world: int) -> dict:
+    """The `config` object of both arms' JSON lines (identical for the same run)."""
+    return {"workload": w.name, "T": w.T, "D": w.D, "F": w.F, "E": w.E, "k": w.k,
+            "shared_expert": w.shared, "l2": L2_NOTE, "parallelism": f"replicas x{world}"}
+
+
+def run_reference(args, w, rank, world):
+    """The reference arm: the fp64 oracle as it stands, on the host cores.
+    Every step runs the whole layer on the first n tokens of the workload; n
+    is sized from a calibration run so that the warm-up and timed steps take
+    about REF_BUDGET_S together (n = T when that fits).  The line reports the
+    time of the steps actually run: ms_per_step is one n-token step, value is
+    n tokens / that time."""
     if rank != 0:
         return
-    L = inputs.make_layer(w)
-    # warm-up runs (not timed), then `steps` timed runs on a bounded sample
     from oracle import moe_oracle as orc
-    n = max(64, min(w.T, 1024))
-    for _ in range(min(args.warmup, 1)):
-        orc.moe_ffn_forward(L["x"][:64], L["Wg"], L["W1"], L["W3"], L["W2"], w.k, bias=L["bias"],
-                            Ws1=L["Ws1"], Ws3=L["Ws3"], Ws2=L["Ws2"])
-    times = []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
+    L = inputs.make_layer(w)
+
+    def run(n):
         orc.moe_ffn_forward(L["x"][:n], L["Wg"], L["W1"], L["W3"], L["W2"], w.k, bias=L["bias"],
                             Ws1=L["Ws1"], Ws3=L["Ws3"], Ws2=L["Ws2"])
+
+    # calibration: a step costs about fixed + per_token * n seconds
+    cal = []
+    for n_cal in (min(w.T, 256), min(w.T, 1024)):
+        t0 = time.perf_counter()
+        run(n_cal)
+        cal.append((n_cal, time.perf_counter() - t0))
+    (n1, t1), (n2, t2) = cal
+    per_token = (t2 - t1) / (n2 - n1) if n2 > n1 else t2 / n2
+    per_token = max(per_token, t2 / n2 / 4)
+    fixed = max(0.0, t2 - per_token * n2)
+    nsteps = max(1, args.steps) + max(0, args.warmup)
+    n = int((REF_BUDGET_S / nsteps - fixed) / per_token) // 64 * 64
+    n = max(min(64, w.T), min(w.T, n))
+    for _ in range(args.warmup):
+        run(n)
+    times = []
+    for _ in range(max(1, args.steps)):
+        t0 = time.perf_counter()
+        run(n)
         times.append(time.perf_counter() - t0)
-        if sum(times) > 120:
-            break
-    tps = n * len(times) / sum(times)
-    sample = f"first {n} of {w.T} tokens per step through the whole layer (fp64 numpy oracle)"
+    step_s = float(np.mean(times))
+    tps = n / step_s
+    sample = (f"the first {n} of the workload's {w.T} tokens through the whole layer per step "
+              f"(fp64 numpy oracle); {len(times)} timed steps")
     line = {
         "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus,
-        "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 * w.T / tps,
+        "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 * step_s,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.name, "T": w.T, "D": w.D, "F": w.F, "E": w.E,
-                                        "k": w.k, "shared_expert": w.shared},
+        "data": "synthetic", "config": line_config(w, world), "sample_tokens": n,
         "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -441,6 +474,105 @@ def run_backward_bench(args, w):
     print(json.dumps(line), flush=True)
 
 
+def time_forward(step, flush_l2, K, W, local_rank, world, dev, moe):
+    """W warm-up steps, then K timed steps (L2 flushed before each, outside
+    the events), then extra steps with an event at every stage boundary for
+    the per-stage breakdown.  The timed steps record only a start and an end
+    event: events between the kernels would re-serialise their programmatic
+    (overlapped) launches.  Returns the mean step time (max over ranks), the
+    per-step times, the mean stage times and the clocks seen."""
+    import torch
+    import torch.distributed as dist
+    for _ in range(W):
+        flush_l2()
+        step()
+    torch.cuda.synchronize()
+    if moe.device_error() != 0:
+        raise RuntimeError("device wait timed out during warm-up")
+    step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    KB = max(3, min(K, 50))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(KB)]
+    for row in step_ev + evs:  # create the CUDA events now, outside the timed loop
+        for ev in row:
+            ev.record()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank).__enter__()
+    n_launch0 = moe.launch_count()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush_l2()
+        step([step_ev[i][0], None, None, None, None, step_ev[i][1]])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    n_launch = moe.launch_count() - n_launch0
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    if moe.device_error() != 0:
+        raise RuntimeError("device wait timed out during the timed steps")
+    step_ms = np.array([step_ev[i][0].elapsed_time(step_ev[i][1]) for i in range(K)])
+    ms = reduce_max(float(step_ms.mean()), dev)
+    for i in range(KB):
+        flush_l2()
+        step(evs[i])
+    torch.cuda.synchronize()
+    st = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(KB)])
+    names = ["route", "permute", "w1w3", "w2", "combine"]
+    return {"ms": ms, "step_ms": step_ms, "stage_ms": {n: float(st[:, j].mean()) for j, n in enumerate(names)},
+            "clocks": clocks, "launches": n_launch, "wall_s": wall, "stage_steps": KB}
+
+
+def roofline_place(w, ms: float, pk: dict) -> dict:
+    """Where one forward step of workload w sits against its roofline: the
+    slower of the active FLOPs at the bf16 peak and the algorithmic bytes
+    (unchained path, every tensor read or written once) at the HBM peak."""
+    fl = active_flops(w)
+    by = sum(stage_bytes(w).values())
+    t_flop = fl / (pk["bf16_tflops"] * 1e12)
+    t_hbm = by / (pk["hbm_gbs"] * 1e9)
+    s = ms / 1e3
+    return {"bound": "tensor" if t_flop >= t_hbm else "hbm", "roofline_us": 1e6 * max(t_flop, t_hbm),
+            "frac": max(t_flop, t_hbm) / s, "frac_tensor": t_flop / s, "frac_hbm": t_hbm / s,
+            "active_gflop": fl / 1e9, "algorithmic_mb": by / 1e6}
+
+
+def measure_other_workloads(names, args, dev, moe, flush_l2, pk) -> dict:
+    """Forward-pass tokens/s, active TFLOP/s and roofline placement of each
+    named workload (1 GPU), timed like the headline workload."""
+    import torch
+    res = {}
+    for name in names:
+        w = inputs.WORKLOADS[name]
+        t_gen = time.perf_counter()
+        L = inputs.make_layer(w)
+        G = {key: to_dev(v, dev) for key, v in L.items()}
+        del L
+        t_gen = time.perf_counter() - t_gen
+        ws = moe.Workspace(w.T, w.D, w.F, w.E, w.k, w.shared, device=dev)
+        out = torch.empty(w.T, w.D, dtype=torch.bfloat16, device=dev)
+
+        def step(events=None, G=G, ws=ws, out=out, w=w):
+            moe.moe_ffn_forward(G["x"], G["Wg"], G["W1"], G["W3"], G["W2"], w.k, bias=G["bias"],
+                                Ws1=G["Ws1"], Ws3=G["Ws3"], Ws2=G["Ws2"], out=out, workspace=ws,
+                                stage_events=events)
+
+        tm = time_forward(step, flush_l2, args.steps, args.warmup, 0, 1, dev, moe)
+        ms = tm["ms"]
+        res[name] = {
+            "T": w.T, "D": w.D, "F": w.F, "E": w.E, "k": w.k, "shared_expert": w.shared,
+            "value": w.T / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "ms_per_step_median": float(np.median(tm["step_ms"])), "steps": args.steps,
+            "active_tflops": active_flops(w) / (ms / 1e3) / 1e12,
+            "roofline": roofline_place(w, ms, pk), "stage_ms": tm["stage_ms"], "clocks": tm["clocks"],
+            "gpu_launches": int(tm["launches"]), "input_generation_s": t_gen,
+        }
+        del G, ws, out, step
+        torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -449,6 +581,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=list(inputs.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip timing the other synthetic workloads after the headline one")
     ap.add_argument("--sweep", choices=["fd", "t", "all", "chained"], default=None,
                     help="roofline placement of the grouped GEMMs over F/D or tokens per expert; "
                          "'chained': chained vs unchained expert FFN (D <= 256)")
@@ -475,7 +609,7 @@ def main():
     w = inputs.WORKLOADS[args.workload]
 
     if args.impl == "reference":
-        run_reference(args, w, rank)
+        run_reference(args, w, rank, world)
         return
 
     import torch
@@ -507,48 +641,10 @@ def main():
                             Ws1=G["Ws1"], Ws3=G["Ws3"], Ws2=G["Ws2"], out=out, workspace=ws,
                             stage_events=events)
 
-    for _ in range(args.warmup):
-        flush_l2()
-        step()
-    torch.cuda.synchronize()
-    if moe.device_error() != 0:
-        raise RuntimeError("device wait timed out during warm-up")
-
+    tm = time_forward(step, flush_l2, args.steps, args.warmup, local_rank, world, dev, moe)
+    ms, step_ms, stage_ms, clocks = tm["ms"], tm["step_ms"], tm["stage_ms"], tm["clocks"]
+    n_launch, wall, KB = tm["launches"], tm["wall_s"], tm["stage_steps"]
     K = args.steps
-    # The timed steps record only a start and an end event: events between
-    # the kernels would re-serialise their programmatic (overlapped) launches.
-    step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    KB = max(3, min(K, 50))  # extra steps with all stage boundaries, for the breakdown
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(KB)]
-    for row in step_ev + evs:  # create the CUDA events now, outside the timed loop
-        for ev in row:
-            ev.record()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    sampler = ClockSampler(local_rank).__enter__()
-    n_launch0 = moe.launch_count()
-    wall0 = time.perf_counter()
-    for i in range(K):
-        flush_l2()
-        step([step_ev[i][0], None, None, None, None, step_ev[i][1]])
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    n_launch = moe.launch_count() - n_launch0
-    clocks = sampler.stop()
-    if world > 1:
-        dist.barrier()
-    if moe.device_error() != 0:
-        raise RuntimeError("device wait timed out during the timed steps")
-    step_ms = np.array([step_ev[i][0].elapsed_time(step_ev[i][1]) for i in range(K)])
-    ms = reduce_max(float(step_ms.mean()), dev)
-
-    # per-stage breakdown (and the duration of the W1||W3 kernel for the roofline)
-    for i in range(KB):
-        flush_l2()
-        step(evs[i])
-    torch.cuda.synchronize()
-    stage_ms = np.array([[evs[i][s].elapsed_time(evs[i][s + 1]) for s in range(5)] for i in range(KB)])
 
     # ---- the same step replayed from a CUDA graph (the L2 flush stays outside) ----
     gs = torch.cuda.Stream(device=dev)
@@ -612,8 +708,7 @@ def main():
     assert torch.equal(out_host[0], out_host[1])  # both pipelines computed the same layer
 
     pk, pk_kind = peaks()
-    names = ["route", "permute", "w1w3", "w2", "combine"]
-    st_mean = {n: float(stage_ms[:, i].mean()) for i, n in enumerate(names)}
+    st_mean = stage_ms
     sb = stage_bytes(w)
     fl = active_flops(w)
     tokens_s = T * world / (ms / 1e3)
@@ -622,6 +717,15 @@ def main():
     traffic = ncu_traffic("grouped_gemm_pair_kernel<true>")
     hbm_stages = st_mean["route"] + st_mean["permute"] + st_mean["combine"]
     hbm_bytes = sb["route"] + sb["permute"] + sb["combine"]
+
+    # ---- the other synthetic workloads, one GPU only (each timed like the headline) ----
+    per_workload = None
+    if world == 1 and not args.no_per_workload:
+        del ws_h, x_host, out_host
+        others = [n for n in inputs.WORKLOAD_ORDER if n != w.name]
+        per_workload = measure_other_workloads(others, args, dev, moe, flush_l2, pk)
+        per_workload[w.name] = {"see": "the headline keys of this line",
+                                "roofline": roofline_place(w, ms, pk)}
 
     if rank != 0:
         if world > 1:
@@ -638,9 +742,7 @@ def main():
         "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "D": w.D, "F": w.F, "E": w.E, "k": w.k,
-                   "shared_expert": w.shared, "l2": "flushed between steps (512 MB write + read back)",
-                   "parallelism": f"replicas x{world}"},
+        "config": line_config(w, world),
         "ms_per_step_median": float(np.median(step_ms)),
         "active_tflops": fl * world / (ms / 1e3) / 1e12,
         "frac_of_bf16_peak": fl / (ms / 1e3) / 1e12 / pk["bf16_tflops"],
@@ -663,6 +765,7 @@ def main():
         "clocks": clocks,
         "wall_s_timed_loop": wall,
         "cpu_baseline": cpu,
+        "per_workload": per_workload,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
