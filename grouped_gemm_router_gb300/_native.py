@@ -63,9 +63,9 @@ _SIGNATURES = {
     "moe_permute_scratch_size": (_sz, [MoeDims]),
     "moe_permute": (_i32, [_vp, MoeDims, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_grouped_swiglu": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, MoeDims, _vp, _vp]),
-    "moe_grouped_down": (_i32, [_vp, _vp, _vp, _vp, MoeDims, _vp, _vp]),
-    "moe_grouped_ffn_chained": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, MoeDims, _vp, _vp]),
-    "moe_combine": (_i32, [_vp, _vp, _vp, MoeDims, _i32, _vp, _vp]),
+    "moe_grouped_down": (_i32, [_vp, _vp, _vp, _vp, MoeDims, _vp, _vp, _vp]),
+    "moe_grouped_ffn_chained": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, MoeDims, _vp, _vp, _vp]),
+    "moe_combine": (_i32, [_vp, _vp, _vp, _vp, MoeDims, _vp, _vp]),
     "moe_permute_noalloc": (_i32, [_vp, MoeDims, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_device_error": (_i32, []),
     "moe_selftest_wait_timeout": (_i32, [_i32, _vp, _vp]),

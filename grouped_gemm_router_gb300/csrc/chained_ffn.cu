@@ -21,8 +21,9 @@
 // accumulator; this is why D <= 256.  The MMA issuer runs
 // G1(0), G1(1), G2(0), G1(2), G2(1), ..., G2(last) and the producer streams
 // the W1/W3 and W2 blocks through one ring in exactly that order.  After the
-// last chunk the epilogue stores Y (bf16) with the row predication of the
-// grouped GEMM (rows past the group's end are not stored).
+// last chunk the epilogue stores Y (bf16; the shared group's rows in fp32)
+// with the row predication of the grouped GEMM (rows past the group's end
+// are not stored).
 //
 // Accumulation order: g/u over k in 16-deep slices, Y over F in 16-deep
 // slices, chunk by chunk -- the same order as the two separate grouped GEMMs,
@@ -84,7 +85,8 @@ struct ChainArgs {
   int T_shared;            // rows of the shared group (0: none)
   int D;
   int F;
-  uint16_t* Y;             // output [S + T_shared, D]
+  uint16_t* Y;             // output of the routed rows [S, D]
+  float* Ys;               // the shared group's output [T_shared, D], fp32
   unsigned int* dev_err;
 };
 
@@ -119,7 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const __grid_constant__ CUtensorMap mapW3s,
                             const __grid_constant__ CUtensorMap mapW2,
                             const __grid_constant__ CUtensorMap mapW2s,
-                            const __grid_constant__ CUtensorMap mapY, const ChainArgs p) {
+                            const __grid_constant__ CUtensorMap mapY,
+                            const __grid_constant__ CUtensorMap mapYs, const ChainArgs p) {
   extern __shared__ uint8_t chain_smem_raw[];
   __shared__ ChainCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -467,10 +470,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = row < nrows_g;
       const int warp_row0 = m * kTileRows + 128 * static_cast<int>(rank) + q * 32;
       const bool full_box = warp_row0 + kOutBoxRows <= nrows_g;
+      const bool f32_rows = g >= p.E;  // the shared expert's rows keep fp32
       for (int cc = part * halfD; cc < (part + 1) * halfD; cc += kOutBoxCols) {
         uint32_t ra[32];
         tmem_ld_32cols(lane_base + kTmemY + cc, ra);
         tmem_ld_wait();
+        if (f32_rows) {
+          if (full_box)
+            store_box_f32_tma(&mapYs, stage_out, ra, cc, warp_row0);
+          else if (valid)
+            store_row_f32(p.Ys + static_cast<size_t>(row) * p.D + cc, ra);
+          continue;
+        }
         uint32_t packed[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j)
@@ -565,15 +576,14 @@ cudaError_t chain_setup(ChainDevice* out) {
 cudaError_t launch_chained_ffn(const uint16_t* x_sorted, const uint16_t* x, const uint16_t* W1,
                                const uint16_t* W3, const uint16_t* W2, const uint16_t* Ws1,
                                const uint16_t* Ws3, const uint16_t* Ws2, const int32_t* offsets,
-                               const moe_dims& d, uint16_t* y, cudaStream_t s, bool pdl) {
+                               const moe_dims& d, uint16_t* y, float* ys, cudaStream_t s, bool pdl) {
   if (d.D > kMaxD || d.D % kBK != 0 || d.F % kFC != 0) return cudaErrorInvalidValue;
   ChainDevice cd;
   cudaError_t e = chain_setup(&cd);
   if (e != cudaSuccess) return e;
   const int S = d.T * d.k;
   const bool shared = Ws1 != nullptr;
-  const uint64_t yrows = static_cast<uint64_t>(S) + (shared ? d.T : 0);
-  CUtensorMap mA, mAs, mW1, mW3, mW1s, mW3s, mW2, mW2s, mY;
+  CUtensorMap mA, mAs, mW1, mW3, mW1s, mW3s, mW2, mW2s, mY, mYs;
   if ((e = tensor_map_2d(&mA, x_sorted, S, d.D, 128, kBK)) != cudaSuccess) return e;
   if ((e = tensor_map_2d(&mW1, W1, static_cast<uint64_t>(d.E) * d.D, d.F, kBK1, 64)) != cudaSuccess) return e;
   if ((e = tensor_map_2d(&mW3, W3, static_cast<uint64_t>(d.E) * d.D, d.F, kBK1, 64)) != cudaSuccess) return e;
@@ -589,7 +599,12 @@ cudaError_t launch_chained_ffn(const uint16_t* x_sorted, const uint16_t* x, cons
     mW3s = mW3;
     mW2s = mW2;
   }
-  if ((e = tensor_map_2d(&mY, y, yrows, d.D, kOutBoxRows, kOutBoxCols)) != cudaSuccess) return e;
+  if ((e = tensor_map_2d(&mY, y, S, d.D, kOutBoxRows, kOutBoxCols)) != cudaSuccess) return e;
+  if (shared) {
+    if ((e = tensor_map_f32_3d(&mYs, ys, d.D, d.T, 1, 16, kOutBoxRows)) != cudaSuccess) return e;
+  } else {
+    mYs = mY;
+  }
   ChainArgs a;
   a.offsets = offsets;
   a.E = d.E;
@@ -598,6 +613,7 @@ cudaError_t launch_chained_ffn(const uint16_t* x_sorted, const uint16_t* x, cons
   a.D = d.D;
   a.F = d.F;
   a.Y = y;
+  a.Ys = ys;
   a.dev_err = cd.dev_err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * cd.pairs, 1, 1);
@@ -613,7 +629,7 @@ cudaError_t launch_chained_ffn(const uint16_t* x_sorted, const uint16_t* x, cons
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  e = cudaLaunchKernelEx(&cfg, chained_ffn_pair_kernel, mA, mAs, mW1, mW3, mW1s, mW3s, mW2, mW2s, mY, a);
+  e = cudaLaunchKernelEx(&cfg, chained_ffn_pair_kernel, mA, mAs, mW1, mW3, mW1s, mW3s, mW2, mW2s, mY, mYs, a);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }

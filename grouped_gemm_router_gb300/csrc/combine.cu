@@ -9,7 +9,9 @@
 // A gather (one warp per token, 16-byte vectors) instead of a scatter with
 // atomics: every output row is written exactly once and the summation order
 // is fixed (j = 0..k-1, then the shared term), so the result is
-// deterministic.
+// deterministic.  The routed rows of y are bf16; the shared expert's rows ys
+// are fp32 (its term enters with weight 1, so its own rounding is kept out of
+// the sum).
 #include "moe_device.cuh"
 #include "moe_kernels.cuh"
 
@@ -36,8 +38,8 @@ MOE_DEV void fma_bf16x8(float (&acc)[8], float w, const uint4& v) {
 // first to leave.
 template <int KMAX, int U>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
-    const uint4* __restrict__ y, const float* __restrict__ w, const int32_t* __restrict__ inv, int T,
-    int D, int k, int S, int has_shared, uint4* __restrict__ out) {
+    const uint4* __restrict__ y, const float4* __restrict__ ys, const float* __restrict__ w,
+    const int32_t* __restrict__ inv, int T, int D, int k, uint4* __restrict__ out) {
   griddep_wait();  // y comes from the previous kernel
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -57,11 +59,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     rows[j] = y + static_cast<size_t>(__shfl_sync(0xffffffffu, my_row, j)) * n16;
     ws[j] = __shfl_sync(0xffffffffu, my_w, j);
   }
-  const uint4* ysh = y + static_cast<size_t>(S + t) * n16;
+  const bool has_shared = ys != nullptr;
+  const float4* ysh = has_shared ? ys + static_cast<size_t>(t) * (2 * n16) : nullptr;
   uint4* orow = out + static_cast<size_t>(t) * n16;
   for (int c0 = lane; c0 < n16; c0 += 32 * U) {
     uint4 v[U][KMAX];
-    uint4 vs[U];
+    float4 vs[U][2];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int c = c0 + 32 * u;
@@ -69,7 +72,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
 #pragma unroll
       for (int j = 0; j < KMAX; ++j)
         if (j < k && in) v[u][j] = __ldcs(rows[j] + c);
-      vs[u] = (has_shared && in) ? __ldcs(ysh + c) : make_uint4(0, 0, 0, 0);
+      if (has_shared && in) {
+        vs[u][0] = __ldcs(ysh + 2 * c);
+        vs[u][1] = __ldcs(ysh + 2 * c + 1);
+      }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -82,12 +88,14 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
       for (int j = 0; j < KMAX; ++j)
         if (j < k) fma_bf16x8(acc, ws[j], v[u][j]);
       if (has_shared) {
-        const uint32_t q4[4] = {vs[u].x, vs[u].y, vs[u].z, vs[u].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          acc[2 * q] += bf16_lo(q4[q]);
-          acc[2 * q + 1] += bf16_hi(q4[q]);
-        }
+        acc[0] += vs[u][0].x;
+        acc[1] += vs[u][0].y;
+        acc[2] += vs[u][0].z;
+        acc[3] += vs[u][0].w;
+        acc[4] += vs[u][1].x;
+        acc[5] += vs[u][1].y;
+        acc[6] += vs[u][1].z;
+        acc[7] += vs[u][1].w;
       }
       uint4 o;
       o.x = pack_bf16x2(acc[0], acc[1]);
@@ -100,21 +108,21 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
 }
 
 template <int KMAX, int U>
-static cudaError_t launch_combine_k(const uint16_t* y, const float* w, const int32_t* inv, const moe_dims& d,
-                                    int has_shared, uint16_t* out, cudaStream_t s, bool pdl) {
+static cudaError_t launch_combine_k(const uint16_t* y, const float* ys, const float* w, const int32_t* inv,
+                                    const moe_dims& d, uint16_t* out, cudaStream_t s, bool pdl) {
   const int grid = (d.T + kCombineWarps - 1) / kCombineWarps;
   return launch_kernel(combine_kernel<KMAX, U>, dim3(grid), dim3(kCombineThreads), 0, s, pdl,
-                       reinterpret_cast<const uint4*>(y), w, inv, d.T, d.D, d.k, d.T * d.k, has_shared,
-                       reinterpret_cast<uint4*>(out));
+                       reinterpret_cast<const uint4*>(y), reinterpret_cast<const float4*>(ys), w, inv, d.T, d.D,
+                       d.k, reinterpret_cast<uint4*>(out));
 }
 
-cudaError_t launch_combine(const uint16_t* y, const float* w, const int32_t* inv, const moe_dims& d,
-                           int has_shared, uint16_t* out, cudaStream_t s, bool pdl) {
-  if (d.k <= 1) return launch_combine_k<1, 4>(y, w, inv, d, has_shared, out, s, pdl);
-  if (d.k <= 2) return launch_combine_k<2, 3>(y, w, inv, d, has_shared, out, s, pdl);
-  if (d.k <= 4) return launch_combine_k<4, 2>(y, w, inv, d, has_shared, out, s, pdl);
-  if (d.k <= 8) return launch_combine_k<8, 1>(y, w, inv, d, has_shared, out, s, pdl);
-  return launch_combine_k<16, 1>(y, w, inv, d, has_shared, out, s, pdl);
+cudaError_t launch_combine(const uint16_t* y, const float* ys, const float* w, const int32_t* inv,
+                           const moe_dims& d, uint16_t* out, cudaStream_t s, bool pdl) {
+  if (d.k <= 1) return launch_combine_k<1, 4>(y, ys, w, inv, d, out, s, pdl);
+  if (d.k <= 2) return launch_combine_k<2, 3>(y, ys, w, inv, d, out, s, pdl);
+  if (d.k <= 4) return launch_combine_k<4, 2>(y, ys, w, inv, d, out, s, pdl);
+  if (d.k <= 8) return launch_combine_k<8, 1>(y, ys, w, inv, d, out, s, pdl);
+  return launch_combine_k<16, 1>(y, ys, w, inv, d, out, s, pdl);
 }
 
 }  // namespace moe

@@ -14,7 +14,9 @@
 //  * Down (W2): y[p] = h[p] W2[e], bf16 out.
 // The always-on shared expert is one more group whose A operand is x itself
 // (SwiGLU) or the shared rows of h (down), and whose B operand is its own
-// weights; its outputs go to rows S .. S + T of h / y.
+// weights; its h goes to rows S .. S + T of h (bf16), its down-projection to
+// ys [T, D] in fp32: it enters the layer's output with weight 1, so it is
+// the one intermediate that keeps its fp32 accumulation.
 //
 // Ragged groups: group g owns rows [row0_g, row0_g + n_g).  Its m-tiles load
 // 256 rows with TMA starting at row0_g + 256 m; rows past the group belong to
@@ -86,7 +88,8 @@ struct GemmArgs {
   int N;                   // output columns
   int tile_n;              // MMA N: SwiGLU 2*hw, down = output tile width
   int shared_a_row0;       // first A row of the shared group in its tensor map
-  uint16_t* C;             // output [S + T_shared, N]
+  uint16_t* C;             // output [S + T_shared, N] (down: [S, N])
+  float* Cs;               // down: the shared group's output [T_shared, N] in fp32
 };
 
 
@@ -138,7 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                              const __grid_constant__ CUtensorMap mapB1,
                              const __grid_constant__ CUtensorMap mapB0_sh,
                              const __grid_constant__ CUtensorMap mapB1_sh,
-                             const __grid_constant__ CUtensorMap mapC, const GemmArgs p) {
+                             const __grid_constant__ CUtensorMap mapC,
+                             const __grid_constant__ CUtensorMap mapCs, const GemmArgs p) {
   extern __shared__ uint8_t gemm_smem_raw[];
   __shared__ PairCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -373,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int warp_row0 = m * kPairBM + 128 * static_cast<int>(rank) + q * 32;
       const bool full_box = warp_row0 + kOutBoxRows <= nrows_g;
       const int col0 = n * hw;
+      const bool f32_rows = !kSwiGLU && g >= p.E;  // the shared expert's down-projection: fp32
       uint16_t* crow = p.C + static_cast<size_t>(ctl.row0[g] + (valid ? row : 0)) * p.N + col0;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * 256;
       const int cols_per_part = hw / kEpiParts;
@@ -405,6 +410,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int b = 0; b < kMaxBoxes; ++b) {
         const int cc = c_first + b * kOutBoxCols;
         if (b >= nbox || col0 + cc >= p.N) break;  // past the group, or past the last column
+        if (!kSwiGLU && f32_rows) {
+          if (full_box)
+            store_box_f32_tma(&mapCs, stage_out, acc[b], col0 + cc, warp_row0);
+          else if (valid)
+            store_row_f32(p.Cs + static_cast<size_t>(row) * p.N + col0 + cc, acc[b]);
+          continue;
+        }
         uint32_t packed[16];
         if (kSwiGLU) {
 #pragma unroll
@@ -525,8 +537,8 @@ DeviceInfo g_dev[64];
 template <bool kSwiGLU>
 cudaError_t launch_pair(int nclusters, const CUtensorMap& a, const CUtensorMap& as,
                         const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b0s,
-                        const CUtensorMap& b1s, const CUtensorMap& c, const GemmArgs& args,
-                        cudaStream_t s, bool pdl) {
+                        const CUtensorMap& b1s, const CUtensorMap& c, const CUtensorMap& cs,
+                        const GemmArgs& args, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * nclusters, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -541,7 +553,7 @@ cudaError_t launch_pair(int nclusters, const CUtensorMap& a, const CUtensorMap& 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kSwiGLU>, a, as, b0, b1, b0s, b1s, c, args);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kSwiGLU>, a, as, b0, b1, b0s, b1s, c, cs, args);
 }
 
 // One-time set-up of the current device (kernel attributes, co-resident
@@ -657,17 +669,18 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
   a.tile_n = 2 * hw;
   a.shared_a_row0 = 0;
   a.C = h;
+  a.Cs = nullptr;
   CUtensorMap mC;
   if ((e = make_map(&mC, h, static_cast<uint64_t>(S) + (shared ? d.T : 0), d.F, kOutBoxRows, kOutBoxCols)) !=
       cudaSuccess)
     return e;
-  e = launch_pair<true>(di.pair_clusters[1], mA, mAs, mB0, mB1, mB0s, mB1s, mC, a, s, pdl);
+  e = launch_pair<true>(di.pair_clusters[1], mA, mAs, mB0, mB1, mB0s, mB1s, mC, mC, a, s, pdl);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uint16_t* Ws2,
-                                const int32_t* offsets, const moe_dims& d, uint16_t* y,
+                                const int32_t* offsets, const moe_dims& d, uint16_t* y, float* ys,
                                 cudaStream_t s, bool pdl) {
   DeviceInfo di;
   cudaError_t e = device_setup(&di);
@@ -695,9 +708,15 @@ cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uin
   a.tile_n = tn;
   a.shared_a_row0 = S;
   a.C = y;
-  CUtensorMap mC;
-  if ((e = make_map(&mC, y, hrows, d.D, kOutBoxRows, kOutBoxCols)) != cudaSuccess) return e;
-  e = launch_pair<false>(di.pair_clusters[0], mA, mA, mB0, mB0, mB0s, mB0s, mC, a, s, pdl);
+  a.Cs = ys;
+  CUtensorMap mC, mCs;
+  if ((e = make_map(&mC, y, S > 0 ? S : 1, d.D, kOutBoxRows, kOutBoxCols)) != cudaSuccess) return e;
+  if (shared) {
+    if ((e = tensor_map_f32_3d(&mCs, ys, d.D, d.T, 1, 16, kOutBoxRows)) != cudaSuccess) return e;
+  } else {
+    mCs = mC;
+  }
+  e = launch_pair<false>(di.pair_clusters[0], mA, mA, mB0, mB0, mB0s, mB0s, mC, mCs, a, s, pdl);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -10,6 +10,17 @@ namespace moe {
 static std::atomic<uint64_t> g_launches{0};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+moe_status check_dims(const moe_dims& d) {
+  if (d.T < 0 || d.D <= 0 || d.F <= 0 || d.E <= 0 || d.k <= 0) return MOE_ERR_INVALID_ARG;
+  if (d.k > d.E) return MOE_ERR_INVALID_ARG;
+  if (d.T > (1 << 24)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d.D % 64 || d.F % 64 || d.D > MOE_MAX_DIM || d.F > MOE_MAX_DIM) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d.E > MOE_MAX_EXPERTS || d.k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -27,6 +38,7 @@ struct Workspace {
   uint16_t* x_sorted;
   uint16_t* h;
   uint16_t* y;
+  float* ys;
   uint16_t* x_stage;
   uint16_t* out_stage;
   size_t bytes;
@@ -46,14 +58,15 @@ Workspace carve(void* base, const moe_dims& d, bool shared, bool host_io) {
   w.wpack = take(route_packed_bytes(d.D, d.E));
   w.ids = reinterpret_cast<int32_t*>(take(S * 4));
   w.w = reinterpret_cast<float*>(take(S * 4));
-  w.hist = reinterpret_cast<int32_t*>(take(static_cast<size_t>(route_blocks(d.T)) * d.E * 4));
+  w.hist = reinterpret_cast<int32_t*>(take(static_cast<size_t>(route_blocks_max(d.T)) * d.E * 4));
   w.counts = reinterpret_cast<int32_t*>(take(static_cast<size_t>(d.E) * 4));
   w.offsets = reinterpret_cast<int32_t*>(take(static_cast<size_t>(d.E + 1) * 4));
   w.perm = reinterpret_cast<int32_t*>(take(S * 4));
   w.inv = reinterpret_cast<int32_t*>(take(S * 4));
   w.x_sorted = reinterpret_cast<uint16_t*>(take(S * d.D * 2));
   w.h = reinterpret_cast<uint16_t*>(take(rows * d.F * 2));
-  w.y = reinterpret_cast<uint16_t*>(take(rows * d.D * 2));
+  w.y = reinterpret_cast<uint16_t*>(take(S * d.D * 2));
+  w.ys = shared ? reinterpret_cast<float*>(take(T * d.D * 4)) : nullptr;
   if (host_io) {
     w.x_stage = reinterpret_cast<uint16_t*>(take(T * d.D * 2));
     w.out_stage = reinterpret_cast<uint16_t*>(take(T * d.D * 2));
@@ -104,22 +117,11 @@ BwdWorkspace carve_bwd(void* base, const moe_dims& d, bool shared) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-moe_status check_dims(const moe_dims& d) {
-  if (d.T < 0 || d.D <= 0 || d.F <= 0 || d.E <= 0 || d.k <= 0) return MOE_ERR_INVALID_ARG;
-  if (d.k > d.E) return MOE_ERR_INVALID_ARG;
-  if (d.T > (1 << 24)) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (d.D % 64 || d.F % 64 || d.D > MOE_MAX_DIM || d.F > MOE_MAX_DIM) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (d.E > MOE_MAX_EXPERTS || d.k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED_SHAPE;
-  return MOE_OK;
-}
-
 // Shared-expert pointers: all three set or all three NULL.
 int shared_state(const void* a, const void* b, const void* c) {
   const int n = (a != nullptr) + (b != nullptr) + (c != nullptr);
   return n == 0 ? 0 : (n == 3 ? 1 : -1);
 }
-
-moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 void record(const moe_ffn_options* o, int i, cudaStream_t s) {
   if (o != nullptr && o->stage_events[i] != nullptr)
@@ -151,18 +153,18 @@ moe_status run_layer(const uint16_t* x, const uint16_t* Wg, const float* bias, c
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(o, 2, s);
   if (o != nullptr && (o->flags & MOE_FFN_CHAINED)) {
-    e = launch_chained_ffn(ws.x_sorted, x, W1, W3, W2, Ws1, Ws3, Ws2, ws.offsets, d, ws.y, s, true);
+    e = launch_chained_ffn(ws.x_sorted, x, W1, W3, W2, Ws1, Ws3, Ws2, ws.offsets, d, ws.y, ws.ys, s, true);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     record(o, 3, s);
   } else {
     e = launch_grouped_swiglu(ws.x_sorted, x, W1, W3, Ws1, Ws3, ws.offsets, d, ws.h, s, true);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     record(o, 3, s);
-    e = launch_grouped_down(ws.h, W2, Ws2, ws.offsets, d, ws.y, s, true);
+    e = launch_grouped_down(ws.h, W2, Ws2, ws.offsets, d, ws.y, ws.ys, s, true);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   record(o, 4, s);
-  e = launch_combine(ws.y, w, ws.inv, d, shared ? 1 : 0, out, s, true);
+  e = launch_combine(ws.y, shared ? ws.ys : nullptr, w, ws.inv, d, out, s, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(o, 5, s);
   return MOE_OK;
@@ -370,7 +372,7 @@ int moe_route_block_tokens(int T) { return route_block_tokens(T); }
 
 size_t moe_permute_scratch_size(moe_dims d) {
   if (check_dims(d) != MOE_OK) return 0;
-  return static_cast<size_t>(route_blocks(d.T)) * d.E * 4;
+  return static_cast<size_t>(route_blocks_max(d.T)) * d.E * 4;
 }
 
 moe_status moe_permute(const int32_t* ids, moe_dims d, int32_t* counts, int32_t* offsets,
@@ -417,14 +419,14 @@ moe_status moe_grouped_swiglu(const void* x_sorted, const void* x, const void* W
 moe_status moe_grouped_ffn_chained(const void* x_sorted, const void* x, const void* W1,
                                    const void* W3, const void* W2, const void* Ws1,
                                    const void* Ws3, const void* Ws2, const int32_t* offsets,
-                                   moe_dims d, void* y, void* stream) {
+                                   moe_dims d, void* y, float* ys, void* stream) {
   moe_status st = check_dims(d);
   if (st != MOE_OK) return st;
   if (d.D > MOE_CHAINED_MAX_D) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!x_sorted || !W1 || !W3 || !W2 || !offsets || !y) return MOE_ERR_INVALID_ARG;
   if (shared_state(Ws1, Ws3, Ws2) < 0) return MOE_ERR_INVALID_ARG;
-  if (Ws1 != nullptr && x == nullptr) return MOE_ERR_INVALID_ARG;
-  const void* ptrs[] = {x_sorted, x, W1, W3, W2, Ws1, Ws3, Ws2, y};
+  if (Ws1 != nullptr && (x == nullptr || ys == nullptr)) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x_sorted, x, W1, W3, W2, Ws1, Ws3, Ws2, y, ys};
   for (const void* p : ptrs)
     if (p != nullptr && !aligned16(p)) return MOE_ERR_INVALID_ARG;
   if (d.T == 0) return MOE_OK;
@@ -433,32 +435,34 @@ moe_status moe_grouped_ffn_chained(const void* x_sorted, const void* x, const vo
       static_cast<const uint16_t*>(W1), static_cast<const uint16_t*>(W3),
       static_cast<const uint16_t*>(W2), static_cast<const uint16_t*>(Ws1),
       static_cast<const uint16_t*>(Ws3), static_cast<const uint16_t*>(Ws2), offsets, d,
-      static_cast<uint16_t*>(y), static_cast<cudaStream_t>(stream)));
+      static_cast<uint16_t*>(y), Ws1 != nullptr ? ys : nullptr, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_grouped_down(const void* h, const void* W2, const void* Ws2, const int32_t* offsets,
-                            moe_dims d, void* y, void* stream) {
+                            moe_dims d, void* y, float* ys, void* stream) {
   moe_status st = check_dims(d);
   if (st != MOE_OK) return st;
   if (!h || !W2 || !offsets || !y) return MOE_ERR_INVALID_ARG;
-  const void* ptrs[] = {h, W2, Ws2, y};
+  if (Ws2 != nullptr && ys == nullptr) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {h, W2, Ws2, y, ys};
   for (const void* p : ptrs)
     if (p != nullptr && !aligned16(p)) return MOE_ERR_INVALID_ARG;
   if (d.T == 0) return MOE_OK;
   return cuda_status(launch_grouped_down(static_cast<const uint16_t*>(h),
                                          static_cast<const uint16_t*>(W2),
                                          static_cast<const uint16_t*>(Ws2), offsets, d,
-                                         static_cast<uint16_t*>(y), static_cast<cudaStream_t>(stream)));
+                                         static_cast<uint16_t*>(y), Ws2 != nullptr ? ys : nullptr,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
-moe_status moe_combine(const void* y, const float* weights, const int32_t* inv, moe_dims d,
-                       int has_shared, void* out, void* stream) {
+moe_status moe_combine(const void* y, const float* ys, const float* weights, const int32_t* inv, moe_dims d,
+                       void* out, void* stream) {
   moe_status st = check_dims(d);
   if (st != MOE_OK) return st;
   if (!y || !weights || !inv || !out) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(y) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(out) || (ys != nullptr && !aligned16(ys))) return MOE_ERR_INVALID_ARG;
   if (d.T == 0) return MOE_OK;
-  return cuda_status(launch_combine(static_cast<const uint16_t*>(y), weights, inv, d, has_shared ? 1 : 0,
+  return cuda_status(launch_combine(static_cast<const uint16_t*>(y), ys, weights, inv, d,
                                     static_cast<uint16_t*>(out), static_cast<cudaStream_t>(stream)));
 }
 

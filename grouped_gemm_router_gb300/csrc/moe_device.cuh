@@ -393,6 +393,47 @@ MOE_DEV float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
 MOE_DEV uint32_t lane_id() { return threadIdx.x & 31u; }
 
+// One epilogue warp's 32 rows x 32 fp32 columns (lane = row; v holds the
+// row's 32 values as bits) stored as two boxes of 16 columns through the
+// warp's 2 KB staging buffer with the 64-byte swizzle (16-byte chunk c of
+// row r at chunk c ^ ((r / 2) % 4)) and TMA stores at (col, row0, 0) of a
+// 3-D fp32 tensor map with a {16, 32, 1} box.  Waits first until the
+// warp's earlier stores have read the buffer.
+MOE_DEV void store_box_f32_tma(const CUtensorMap* map, uint8_t* stage, const uint32_t (&v)[32], int col,
+                               int row0) {
+  const uint32_t lane = lane_id();
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4* dst = reinterpret_cast<uint4*>(stage + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4));
+      *dst = make_uint4(v[16 * half + 4 * c], v[16 * half + 4 * c + 1], v[16 * half + 4 * c + 2],
+                        v[16 * half + 4 * c + 3]);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                       reinterpret_cast<uint64_t>(map)),
+                   "r"(col + 16 * half), "r"(row0), "r"(0), "r"(static_cast<uint32_t>(__cvta_generic_to_shared(stage)))
+                   : "memory");
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+  }
+}
+
+// The same 32 fp32 values of one row stored straight to global memory
+// (rows of a box that crosses the end of a group).
+MOE_DEV void store_row_f32(float* dst, const uint32_t (&v)[32]) {
+  float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    d4[c] = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]), __uint_as_float(v[4 * c + 2]),
+                        __uint_as_float(v[4 * c + 3]));
+}
+
 // Programmatic dependent launch: wait until the preceding kernel of the
 // stream has completed and its writes are visible (returns at once when this
 // kernel was not launched as a programmatic dependent) ...

@@ -14,6 +14,11 @@ namespace moe {
 // Counts kernel launches (moe_launch_count).
 void note_launch();
 
+// Host-side checks shared by every entry point (moe_api.cu): the shape
+// limits of the header, and a CUDA error mapped to MOE_ERR_CUDA.
+moe_status check_dims(const moe_dims& d);
+moe_status cuda_status(cudaError_t e);
+
 // Launches `kernel` on `s`; with `pdl` it may start while the previous kernel
 // of the stream finishes (it calls griddep_wait before reading that kernel's
 // results).
@@ -36,8 +41,10 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 }
 
 // ---- routing / permutation (route_permute.cu) ----
-int route_block_tokens(int T);  // tokens per router / permutation block (16, 32 or 64)
-int route_blocks(int T);        // ceil(T / route_block_tokens(T))
+int current_device_sms();       // SM count of the current device (0: none)
+int route_block_tokens(int T);  // tokens per permutation block / histogram row (16, 32 or 64)
+int route_blocks(int T);        // ceil(T / route_block_tokens(T)) on the current device
+int route_blocks_max(int T);    // ceil(T / 16): the most histogram rows on any device
 size_t route_packed_bytes(int D, int E);  // router weights in MMA fragment order
 // Packs Wg into wpack_buf (route_packed_bytes bytes), then routes.
 cudaError_t launch_route(const uint16_t* x, const uint16_t* Wg, const float* bias, const moe_dims& d,
@@ -50,8 +57,9 @@ cudaError_t launch_scatter(const int32_t* ids, const int32_t* hist, const moe_di
                            uint16_t* x_sorted, cudaStream_t s, bool pdl = false);
 
 // ---- combine (combine.cu) ----
-cudaError_t launch_combine(const uint16_t* y, const float* w, const int32_t* inv, const moe_dims& d,
-                           int has_shared, uint16_t* out, cudaStream_t s, bool pdl = false);
+// ys: the shared expert's rows [T, D] fp32, or nullptr without it.
+cudaError_t launch_combine(const uint16_t* y, const float* ys, const float* w, const int32_t* inv,
+                           const moe_dims& d, uint16_t* out, cudaStream_t s, bool pdl = false);
 
 // ---- grouped GEMMs (grouped_gemm.cu) ----
 // W1||W3 with SwiGLU epilogue: A = x_sorted [S, D] (+ x [T, D] for the shared
@@ -60,19 +68,21 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
                                   const uint16_t* W3, const uint16_t* Ws1, const uint16_t* Ws3,
                                   const int32_t* offsets, const moe_dims& d, uint16_t* h,
                                   cudaStream_t s, bool pdl = false);
-// W2: A = h [S (+T), F], B = W2 [E, F, D] (+ Ws2 [F, D]), C = y [S (+T), D].
+// W2: A = h [S (+T), F], B = W2 [E, F, D] (+ Ws2 [F, D]), C = y [S, D] bf16
+// and (with Ws2) ys [T, D] fp32.
 cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uint16_t* Ws2,
-                                const int32_t* offsets, const moe_dims& d, uint16_t* y,
+                                const int32_t* offsets, const moe_dims& d, uint16_t* y, float* ys,
                                 cudaStream_t s, bool pdl = false);
 
 // W1||W3 + SiLU*mul and W2 chained in one kernel (chained_ffn.cu): same
-// inputs as the two grouped GEMMs, y [S (+T), D] out, h never stored.
+// inputs as the two grouped GEMMs, y [S, D] bf16 and (shared) ys [T, D] fp32
+// out, h never stored.
 // Requires D <= kChainedMaxD.
 constexpr int kChainedMaxD = 256;
 cudaError_t launch_chained_ffn(const uint16_t* x_sorted, const uint16_t* x, const uint16_t* W1,
                                const uint16_t* W3, const uint16_t* W2, const uint16_t* Ws1,
                                const uint16_t* Ws3, const uint16_t* Ws2, const int32_t* offsets,
-                               const moe_dims& d, uint16_t* y, cudaStream_t s, bool pdl = false);
+                               const moe_dims& d, uint16_t* y, float* ys, cudaStream_t s, bool pdl = false);
 
 // ---- backward (grouped_gemm_bwd.cu, backward.cu) ----
 // Padded sorted layout of the gradient buffers: group e at rows

@@ -11,8 +11,10 @@
 //
 // Properties of the shared scratch array:
 //  * Size: kNoAllocHistEntries int32 (256 KB).  Every GPU that loads the
-//    library holds it until the process exits.  Calls needing more than that,
-//    ceil(T / 64) * E entries, are rejected with MOE_ERR_UNSUPPORTED_SHAPE.
+//    library holds it until the process exits.  A call needs ceil(T / TB) * E
+//    entries, TB = moe_route_block_tokens(T) on the current device (16, 32 or
+//    64 tokens); calls needing more than the array holds are rejected with
+//    MOE_ERR_UNSUPPORTED_SHAPE.
 //  * Every call on a device shares the one array, and it keeps the previous
 //    call's contents.  Nothing in it has to start at zero: the histogram
 //    kernel writes every entry the call reads.  Calls whose work overlaps on
@@ -65,11 +67,8 @@ using namespace moe;
 extern "C" moe_status moe_permute_noalloc(const int32_t* ids, moe_dims d, int32_t* counts,
                                           int32_t* offsets, int32_t* perm, int32_t* inv,
                                           const void* x, void* x_sorted, void* stream) {
-  if (d.T < 0 || d.D <= 0 || d.F <= 0 || d.E <= 0 || d.k <= 0 || d.k > d.E)
-    return MOE_ERR_INVALID_ARG;
-  if (d.T > (1 << 24) || d.D % 64 || d.F % 64 || d.D > MOE_MAX_DIM || d.F > MOE_MAX_DIM ||
-      d.E > MOE_MAX_EXPERTS || d.k > MOE_MAX_TOPK)
-    return MOE_ERR_UNSUPPORTED_SHAPE;
+  const moe_status st = check_dims(d);  // the same shape limits as moe_permute
+  if (st != MOE_OK) return st;
   if (!ids || !counts || !offsets || !perm || !inv) return MOE_ERR_INVALID_ARG;
   if ((x == nullptr) != (x_sorted == nullptr)) return MOE_ERR_INVALID_ARG;
   if (x && ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(x_sorted)) & 15u))
@@ -85,8 +84,6 @@ extern "C" moe_status moe_permute_noalloc(const int32_t* ids, moe_dims d, int32_
   int32_t* hist = nullptr;
   if (scratch_address(&hist) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_hist(ids, d, hist, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_scatter(ids, hist, d, counts, offsets, perm, inv, static_cast<const uint16_t*>(x),
-                     static_cast<uint16_t*>(x_sorted), s) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return MOE_OK;
+  return cuda_status(launch_scatter(ids, hist, d, counts, offsets, perm, inv, static_cast<const uint16_t*>(x),
+                                    static_cast<uint16_t*>(x_sorted), s));
 }

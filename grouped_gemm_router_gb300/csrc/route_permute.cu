@@ -20,11 +20,27 @@ namespace moe {
 
 constexpr int kRouteThreads = 256;  // 8 warps per router block
 
-// Tokens per router / permutation block: 64 when that still gives every SM two
-// blocks, else 32 or 16, so that small batches spread over the whole GPU.
+// SM count of the current device, cached per device; 0 when it cannot be read.
+int current_device_sms() {
+  static int sms[64] = {0};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (sms[dev] == 0 && cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms[dev] = 0;
+  return sms[dev];
+}
+
+// Tokens per router / permutation block on the current device: 64 when that
+// still gives every SM two blocks, else 32 or 16, so that small batches spread
+// over the whole GPU.  16 when the device cannot be queried (the most blocks,
+// which every workspace is sized for).
 int route_block_tokens(int T) {
-  if (T >= 64 * 2 * 152) return 64;
-  if (T >= 32 * 2 * 152) return 32;
+  const int sms = current_device_sms();
+  if (sms <= 0) return 16;
+  if (T >= 64 * 2 * sms) return 64;
+  if (T >= 32 * 2 * sms) return 32;
   return 16;
 }
 
@@ -32,6 +48,8 @@ int route_blocks(int T) {
   const int tb = route_block_tokens(T);
   return (T + tb - 1) / tb;
 }
+
+int route_blocks_max(int T) { return (T + 15) / 16; }
 
 // Expert tiles of 8 (the MMA's N) for E experts, padded to the instantiated widths.
 int route_expert_tiles(int E) {

@@ -64,7 +64,8 @@ class Workspace:
         T, D, F, E, k = self.dims
         S = T * k
         rows = S + (T if self.shared else 0)
-        nblk = N.route_blocks(T)
+        nblk = N.route_blocks(T)           # rows in use on this device
+        nblk_max = (T + 15) // 16           # rows reserved (16-token blocks)
         out, off = {}, 0
 
         def take(name, n, dtype, shape):
@@ -77,14 +78,17 @@ class Workspace:
         take("router_packed", npack, torch.uint8, (npack,))
         take("ids", S, torch.int32, (T, k))
         take("w", S, torch.float32, (T, k))
-        take("hist", nblk * E, torch.int32, (nblk, E))
+        take("hist", nblk_max * E, torch.int32, (nblk_max, E))
+        out["hist"] = out["hist"][:nblk]
         take("counts", E, torch.int32, (E,))
         take("offsets", E + 1, torch.int32, (E + 1,))
         take("perm", S, torch.int32, (S,))
         take("inv", S, torch.int32, (S,))
         take("x_sorted", S * D, torch.bfloat16, (S, D))
         take("h", rows * F, torch.bfloat16, (rows, F))
-        take("y", rows * D, torch.bfloat16, (rows, D))
+        take("y", S * D, torch.bfloat16, (S, D))
+        if self.shared:
+            take("ys", T * D, torch.float32, (T, D))
         return out
 
 
@@ -296,8 +300,9 @@ def moe_grouped_swiglu(x_sorted, offsets, W1, W3, T, k, x=None, Ws1=None, Ws3=No
     return h
 
 
-def moe_grouped_down(h, offsets, W2, T, k, Ws2=None, y=None):
-    """y [T*k (+T), D] = h W2[e] per expert group (+ shared rows with Ws2)."""
+def moe_grouped_down(h, offsets, W2, T, k, Ws2=None, y=None, ys=None):
+    """(y [T*k, D] bf16, ys [T, D] fp32 or None): y = h W2[e] per expert
+    group; with Ws2, ys = the shared rows of h times Ws2."""
     E, F, D = W2.shape
     shared = Ws2 is not None
     rows = T * k + (T if shared else 0)
@@ -306,17 +311,23 @@ def moe_grouped_down(h, offsets, W2, T, k, Ws2=None, y=None):
     _need(Ws2, "Ws2", torch.bfloat16, (F, D))
     _need(offsets, "offsets", torch.int32, (E + 1,))
     if y is None:
-        y = torch.empty(rows, D, dtype=torch.bfloat16, device=h.device)
+        y = torch.empty(T * k, D, dtype=torch.bfloat16, device=h.device)
+    if shared and ys is None:
+        ys = torch.empty(T, D, dtype=torch.float32, device=h.device)
+    _need(y, "y", torch.bfloat16, (T * k, D))
+    if shared:
+        _need(ys, "ys", torch.float32, (T, D))
     st = lib.moe_grouped_down(_ptr(h), _ptr(W2), _ptr(Ws2), _ptr(offsets), N.dims(T, D, F, E, k),
-                              _ptr(y), _stream())
+                              _ptr(y), _ptr(ys if shared else None), _stream())
     check(st, "moe_grouped_down")
-    return y
+    return y, (ys if shared else None)
 
 
 def moe_grouped_ffn_chained(x_sorted, offsets, W1, W3, W2, T, k, x=None, Ws1=None, Ws3=None,
-                            Ws2=None, y=None):
-    """y [T*k (+T), D] = (silu(A W1[e]) * (A W3[e])) W2[e] per expert group
-    (+ shared rows), in one kernel that never writes h (D <= 256)."""
+                            Ws2=None, y=None, ys=None):
+    """(y [T*k, D] bf16, ys [T, D] fp32 or None) = (silu(A W1[e]) * (A W3[e]))
+    W2[e] per expert group (+ the shared expert's rows), in one kernel that
+    never writes h (D <= 256)."""
     S, D = x_sorted.shape
     E, _, F = W1.shape
     shared = Ws1 is not None
@@ -330,27 +341,32 @@ def moe_grouped_ffn_chained(x_sorted, offsets, W1, W3, W2, T, k, x=None, Ws1=Non
         _need(Ws1, "Ws1", torch.bfloat16, (D, F))
         _need(Ws3, "Ws3", torch.bfloat16, (D, F))
         _need(Ws2, "Ws2", torch.bfloat16, (F, D))
-    rows = T * k + (T if shared else 0)
     if y is None:
-        y = torch.empty(rows, D, dtype=torch.bfloat16, device=x_sorted.device)
+        y = torch.empty(T * k, D, dtype=torch.bfloat16, device=x_sorted.device)
+    if shared and ys is None:
+        ys = torch.empty(T, D, dtype=torch.float32, device=x_sorted.device)
+    _need(y, "y", torch.bfloat16, (T * k, D))
+    if shared:
+        _need(ys, "ys", torch.float32, (T, D))
     st = lib.moe_grouped_ffn_chained(_ptr(x_sorted), _ptr(x), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(Ws1),
                                      _ptr(Ws3), _ptr(Ws2), _ptr(offsets), N.dims(T, D, F, E, k), _ptr(y),
-                                     _stream())
+                                     _ptr(ys if shared else None), _stream())
     check(st, "moe_grouped_ffn_chained")
-    return y
+    return y, (ys if shared else None)
 
 
-def moe_combine(y, weights, inv, has_shared, out=None):
-    """out[t] = sum_j weights[t, j] * y[inv[t*k + j]] (+ y[T*k + t])."""
+def moe_combine(y, weights, inv, ys=None, out=None):
+    """out[t] = sum_j weights[t, j] * y[inv[t*k + j]] (+ ys[t], fp32)."""
     T, k = weights.shape
     D = y.shape[1]
-    _need(y, "y", torch.bfloat16)
+    _need(y, "y", torch.bfloat16, (T * k, D))
+    _need(ys, "ys", torch.float32, (T, D))
     _need(weights, "weights", torch.float32, (T, k))
     _need(inv, "inv", torch.int32, (T * k,))
     if out is None:
         out = torch.empty(T, D, dtype=torch.bfloat16, device=y.device)
     E = max(k, 1)
-    st = lib.moe_combine(_ptr(y), _ptr(weights), _ptr(inv), N.dims(T, D, 64, E, k), int(bool(has_shared)),
+    st = lib.moe_combine(_ptr(y), _ptr(ys), _ptr(weights), _ptr(inv), N.dims(T, D, 64, E, k),
                          _ptr(out), _stream())
     check(st, "moe_combine")
     return out

@@ -96,9 +96,11 @@ typedef struct {
  * device staging buffers used by moe_ffn_forward_host).  The workspace holds,
  * each 256-byte aligned: the packed router weights (moe_route_scratch_size
  * bytes), ids [T,k] i32, w [T,k] f32, block histogram
- * [ceil(T/TB), E] i32 (TB = moe_route_block_tokens(T)), counts [E] i32, offsets [E+1] i32, perm [T*k] i32,
+ * [ceil(T/16), E] i32 (of which the first ceil(T/TB) rows are used, TB =
+ * moe_route_block_tokens(T)), counts [E] i32, offsets [E+1] i32, perm [T*k] i32,
  * inv [T*k] i32, x_sorted [T*k, D] bf16, h [T*k (+T), F] bf16,
- * y [T*k (+T), D] bf16, then (host_io) x [T, D] and out [T, D] bf16. */
+ * y [T*k, D] bf16, (shared) ys [T, D] fp32, then (host_io) x [T, D] and
+ * out [T, D] bf16. */
 size_t moe_ffn_workspace_size(moe_dims d, int has_shared, int host_io);
 
 /* Forward pass of one MoE SwiGLU FFN layer.
@@ -196,11 +198,14 @@ moe_status moe_route(const void* x, const void* Wg, const float* router_bias, mo
                      int32_t* ids, float* weights, int32_t* block_hist, void* scratch,
                      size_t scratch_bytes, void* stream);
 
-/* Tokens per block of the router and permutation kernels for a batch of T
- * tokens: 64, or 32 / 16 for batches too small to give every SM two blocks. */
+/* Tokens per row of the block histogram (and per block of the permutation
+ * kernel) for a batch of T tokens on the current device: 64, or 32 / 16 for
+ * batches too small to give each of the device's SMs two blocks; 16 when no
+ * device can be queried. */
 int moe_route_block_tokens(int T);
 
-/* Scratch bytes moe_permute needs: the block histogram, ceil(T/TB)*E int32. */
+/* Scratch bytes moe_permute needs: the block histogram, sized for the most
+ * rows any device uses, ceil(T/16)*E int32. */
 size_t moe_permute_scratch_size(moe_dims d);
 
 /* Stable permutation of the T*k slots by expert id (section "PyTorch MoE
@@ -224,32 +229,36 @@ moe_status moe_grouped_swiglu(const void* x_sorted, const void* x, const void* W
                               const void* Ws1, const void* Ws3, const int32_t* offsets,
                               moe_dims d, void* h, void* stream);
 
-/* Grouped GEMM W2: y[p] = h[p] W2[e] for the routed rows, and (Ws2 non-NULL)
- * y[T*k + t] = h[T*k + t] Ws2.  y holds T*k (+T) rows of D bf16. */
+/* Grouped GEMM W2: y[p] = h[p] W2[e] for the routed rows, y [T*k, D] bf16;
+ * with the shared expert (Ws2 non-NULL) also ys[t] = h[T*k + t] Ws2, ys
+ * [T, D] fp32 (required then, ignored otherwise).  The shared expert's output
+ * is added to the layer's output with weight 1, so it keeps its fp32
+ * accumulation instead of being rounded to bf16 first. */
 moe_status moe_grouped_down(const void* h, const void* W2, const void* Ws2, const int32_t* offsets,
-                            moe_dims d, void* y, void* stream);
+                            moe_dims d, void* y, float* ys, void* stream);
 
 /* W1||W3 + SiLU*mul and W2 chained in one kernel, h never written to memory
  * ("Chinchilla scaling, MoE, and fused Triton kernels", sections "Fused Triton
  * kernel mechanism" and "Triton fused kernel implementation").  Same inputs as
- * moe_grouped_swiglu and moe_grouped_down together, same output y [T*k (+T), D]
- * bf16: per 256-row tile the kernel streams F in 64-column chunks, rounds each
- * h chunk to bf16 in shared memory and accumulates y in fp32 over the chunks
- * in the order of the two separate GEMMs, so y equals their result.
+ * moe_grouped_swiglu and moe_grouped_down together, same outputs y [T*k, D]
+ * bf16 and (shared) ys [T, D] fp32: per 256-row tile the kernel streams F in
+ * 64-column chunks, rounds each h chunk to bf16 in shared memory and
+ * accumulates y in fp32 over the chunks in the order of the two separate
+ * GEMMs, so y and ys equal their result.
  * MOE_ERR_UNSUPPORTED_SHAPE when D > MOE_CHAINED_MAX_D: a tile's y
  * accumulator (D fp32 columns per row) and two g|u buffers (128 columns each)
  * must fit in the 512 TMEM columns of an SM. */
 moe_status moe_grouped_ffn_chained(const void* x_sorted, const void* x, const void* W1,
                                    const void* W3, const void* W2, const void* Ws1,
                                    const void* Ws3, const void* Ws2, const int32_t* offsets,
-                                   moe_dims d, void* y, void* stream);
+                                   moe_dims d, void* y, float* ys, void* stream);
 
 /* Weighted combine ("PyTorch MoE implementation": inverse permutation and
- * weighted sum): out[t] = sum_j weights[t, j] * y[inv[t*k + j]]
- * (+ y[T*k + t] when has_shared), summed in fp32 in order j = 0..k-1 and then
- * the shared term, rounded once to bf16. */
-moe_status moe_combine(const void* y, const float* weights, const int32_t* inv, moe_dims d,
-                       int has_shared, void* out, void* stream);
+ * weighted sum): out[t] = sum_j weights[t, j] * y[inv[t*k + j]] (+ ys[t] when
+ * ys, the shared expert's rows [T, D] fp32, is non-NULL), summed in fp32 in
+ * order j = 0..k-1 and then the shared term, rounded once to bf16. */
+moe_status moe_combine(const void* y, const float* ys, const float* weights, const int32_t* inv, moe_dims d,
+                       void* out, void* stream);
 
 /* ---- Allocation-free variant ---- */
 

@@ -75,15 +75,18 @@ def test_argument_validation_before_launch(native):
                              p(FAKE), 4, None) == N.MOE_ERR_WORKSPACE
     assert N.lib.moe_grouped_swiglu(p(FAKE), None, p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), good,
                                     p(FAKE), None) == N.MOE_ERR_INVALID_ARG     # shared needs x
-    assert N.lib.moe_combine(p(FAKE), p(FAKE), p(FAKE), N.dims(4, 96, 64, 4, 2), 0, p(FAKE),
+    assert N.lib.moe_combine(p(FAKE), None, p(FAKE), p(FAKE), N.dims(4, 96, 64, 4, 2), p(FAKE),
                              None) == N.MOE_ERR_UNSUPPORTED_SHAPE
+    assert N.lib.moe_grouped_down(p(FAKE), p(FAKE), p(FAKE), p(FAKE), good, p(FAKE), None,
+                                  None) == N.MOE_ERR_INVALID_ARG     # the shared expert needs ys
     # the chained kernel keeps a D-column fp32 accumulator in TMEM: D <= 256
-    chained = lambda d, x=FAKE, shared=(None, None, None): N.lib.moe_grouped_ffn_chained(
+    chained = lambda d, x=FAKE, shared=(None, None, None), ys=FAKE: N.lib.moe_grouped_ffn_chained(
         p(FAKE), p(x) if x else None, p(FAKE), p(FAKE), p(FAKE), *(p(s) if s else None for s in shared),
-        p(FAKE), d, p(FAKE), None)
+        p(FAKE), d, p(FAKE), p(ys) if ys else None, None)
     assert chained(N.dims(256, 320, 256, 4, 2)) == N.MOE_ERR_UNSUPPORTED_SHAPE
     assert chained(good, x=0, shared=(FAKE, FAKE, FAKE)) == N.MOE_ERR_INVALID_ARG   # shared needs x
     assert chained(good, shared=(FAKE, FAKE, None)) == N.MOE_ERR_INVALID_ARG        # partial shared
+    assert chained(good, shared=(FAKE, FAKE, FAKE), ys=0) == N.MOE_ERR_INVALID_ARG  # shared needs ys
     assert chained(N.dims(0, 128, 256, 4, 2)) == N.MOE_OK
     opts = N.MoeOptions()
     opts.flags = N.MOE_FFN_CHAINED
@@ -144,12 +147,11 @@ def test_workspace_size_matches_documented_layout(native):
         a = lambda n: (n + 255) // 256 * 256
         S = T * k
         rows = S + (T if shared else 0)
-        tb = 64 if T >= 64 * 2 * 152 else 32 if T >= 32 * 2 * 152 else 16
-        nblk = (T + tb - 1) // tb
+        nblk = (T + 15) // 16        # histogram rows for the smallest block (16 tokens)
         et = (E + 7) // 8
         et = et if et <= 2 else 4 if et <= 4 else 8 if et <= 8 else 16
         n = a((D // 32) * et * 32 * 16) + a(S * 4) * 2 + a(nblk * E * 4) + a(E * 4) + a((E + 1) * 4) + a(S * 4) * 2
-        n += a(S * D * 2) + a(rows * F * 2) + a(rows * D * 2)
+        n += a(S * D * 2) + a(rows * F * 2) + a(S * D * 2) + (a(T * D * 4) if shared else 0)
         if host_io:
             n += 2 * a(T * D * 2)
         return n
@@ -161,9 +163,10 @@ def test_workspace_size_matches_documented_layout(native):
     assert native.lib.moe_ffn_workspace_size(native.dims(10, 100, 64, 4, 2), 0, 0) == 0
 
 
-def test_route_block_tokens(native):
-    assert [native.lib.moe_route_block_tokens(T) for T in (1, 2048, 9727, 9728, 19455, 19456, 32768)] == \
-        [16, 16, 16, 32, 32, 64, 64]
+def test_permute_scratch_covers_every_device(native):
+    # sized for 16-token blocks, the most histogram rows any device uses
+    for T, E in [(1, 4), (2048, 64), (32768, 8), (65536, 128)]:
+        assert native.lib.moe_permute_scratch_size(native.dims(T, 64, 64, E, 1)) == (T + 15) // 16 * E * 4
 
 
 def test_product_path_fails_loudly_without_library(tmp_path):

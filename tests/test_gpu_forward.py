@@ -17,9 +17,26 @@ from _util import assert_close, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
 
-# workloads small enough for the whole-layer oracle; the others are sampled
-FULL_ORACLE = {"tiny", "small_chunk"}
-SAMPLE_TOKENS = 384
+# every token is compared with the oracle on these workloads (a few seconds of
+# oracle time each); on `wide` the compared tokens are those with a slot in
+# the first or last 256-row tile of some expert's group (whole output tiles of
+# the grouped GEMMs), plus the first and last token and the near-tie tokens
+FULL_ORACLE = {"tiny", "gptoss_lite", "skewed", "small_chunk"}
+TILE_ROWS = 256
+
+
+def _tile_tokens(offsets, perm, k):
+    """Tokens owning a slot in the first or last TILE_ROWS-row tile of each
+    non-empty group of the expert-sorted order."""
+    toks = []
+    for e in range(len(offsets) - 1):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b == a:
+            continue
+        last = a + ((b - a - 1) // TILE_ROWS) * TILE_ROWS
+        for t0 in sorted({a, last}):
+            toks.append(np.asarray(perm[t0:min(t0 + TILE_ROWS, b)], dtype=np.int64) // k)
+    return np.concatenate(toks)
 
 
 @pytest.fixture(scope="module")
@@ -76,9 +93,9 @@ def test_forward_workload(moe, name):
     if name in FULL_ORACLE:
         tokens = np.arange(T)
     else:
-        rng = np.random.default_rng(w_.seed)
-        tokens = np.unique(np.concatenate([rng.choice(T, SAMPLE_TOKENS, replace=False),
+        tokens = np.unique(np.concatenate([_tile_tokens(pm["offsets"], pm["perm"], k),
                                            [0, T - 1], np.nonzero(near)[0]]))
+    print(f"{name}: {tokens.size} of {T} tokens compared with the oracle")
     ref = _oracle(L, k, tokens)
     got = to_f64(out)[tokens]
     same = ~mism[tokens]

@@ -45,10 +45,12 @@ ROUTE_CASES = [
     (333, 192, 64, 20, 5, False, 3, None),          # E padded to 24
     (300, 512, 64, 64, 4, False, 4, None),
     (200, 384, 64, 128, 16, False, 5, None),        # widest router, largest k
-    (257, 4608, 64, 8, 2, False, 6, None),          # D larger than one staged chunk for E=8? no; long D
+    (257, 4608, 64, 8, 2, False, 6, None),          # long D: 6 stages per 16-token tile
     (500, 768, 64, 8, 2, False, 7, inputs.zipf_router_bias(8, 1.2, 7)),
     (12000, 768, 64, 8, 2, False, 8, None),         # 32-token blocks
     (20000, 256, 64, 16, 2, False, 9, None),        # 64-token blocks
+    (40000, 2048, 64, 16, 2, False, 10, None),      # 4 stages per tile, ~16 tiles per CTA
+    (3000, 2048, 64, 128, 8, False, 11, None),      # router weights too large to stage in smem
 ]
 
 
@@ -73,6 +75,15 @@ def test_route(moe, case):
     for b in range(hist.shape[0]):  # per-block histogram of the GPU's own ids
         blk = ids[b * tb:(b + 1) * tb].reshape(-1)
         assert (hist[b] == np.bincount(blk, minlength=E)).all()
+
+
+def test_route_block_tokens_follow_the_sm_count(moe):
+    """64-token blocks when that still gives every SM two of them, else 32 or 16."""
+    from grouped_gemm_router_gb300 import _native
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for T in (1, 2048, 32 * 2 * sms - 1, 32 * 2 * sms, 64 * 2 * sms - 1, 64 * 2 * sms, 32768, 1 << 20):
+        want = 64 if T >= 64 * 2 * sms else 32 if T >= 32 * 2 * sms else 16
+        assert int(_native.lib.moe_route_block_tokens(T)) == want, T
 
 
 def test_route_all_ties_pick_lowest_experts(moe):
@@ -164,18 +175,18 @@ def test_grouped_gemms(moe, case):
         hs_ref = orc.silu(x64 @ orc.bf16_to_f64(L["Ws1"])) * (x64 @ orc.bf16_to_f64(L["Ws3"]))
         assert_close(h_got[S:], hs_ref, "h (shared)", atol=H_ATOL, rtol=H_RTOL)
     # down projection on the GPU's own (bf16) h
-    y = moe.moe_grouped_down(h, offs, to_dev(L["W2"]), T, k, Ws2=to_dev(L["Ws2"]))
+    y, ys = moe.moe_grouped_down(h, offs, to_dev(L["W2"]), T, k, Ws2=to_dev(L["Ws2"]))
     torch.cuda.synchronize()
     y_ref = orc.grouped_down(h_got[:S], orc.bf16_to_f64(L["W2"]), pm["offsets"])
     y_got = to_f64(y)
-    assert_close(y_got[:S], y_ref, "y (routed)", atol=H_ATOL, rtol=H_RTOL)
-    if shared:
-        assert_close(y_got[S:], h_got[S:] @ orc.bf16_to_f64(L["Ws2"]), "y (shared)", atol=H_ATOL, rtol=H_RTOL)
-    # combine on the GPU's own y
-    out = moe.moe_combine(y, to_dev(w.astype(np.float32)), to_dev(pm["inv"]), shared)
+    assert_close(y_got, y_ref, "y (routed)", atol=H_ATOL, rtol=H_RTOL)
+    ys_got = to_f64(ys) if shared else None
+    if shared:   # fp32 accumulation of the bf16 h and Ws2 products, not rounded to bf16
+        assert_close(ys_got, h_got[S:] @ orc.bf16_to_f64(L["Ws2"]), "ys (shared)", atol=1e-4, rtol=1e-4)
+    # combine on the GPU's own y and ys
+    out = moe.moe_combine(y, to_dev(w.astype(np.float32)), to_dev(pm["inv"]), ys=ys)
     torch.cuda.synchronize()
-    out_ref = orc.combine(y_got[:S], pm["inv"], w.astype(np.float32).astype(np.float64),
-                          y_got[S:] if shared else None)
+    out_ref = orc.combine(y_got, pm["inv"], w.astype(np.float32).astype(np.float64), ys_got)
     assert_close(to_f64(out), out_ref, "combine", atol=1e-3, rtol=4e-3)
     assert moe.device_error() == 0
 
@@ -186,13 +197,14 @@ def test_combine_exact_small(moe):
     T, D, k = 70, 64, 3
     rng = np.random.default_rng(1)
     S = T * k
-    y = (rng.integers(-64, 64, size=(S + T, D)) / 16.0).astype(np.float32)
+    y = (rng.integers(-64, 64, size=(S, D)) / 16.0).astype(np.float32)
+    ys = (rng.integers(-4096, 4096, size=(T, D)) / 1024.0).astype(np.float32)   # exact in fp32, not in bf16
     perm = rng.permutation(S).astype(np.int32)
     inv = np.empty(S, np.int32)
     inv[perm] = np.arange(S, dtype=np.int32)
     w = (rng.integers(1, 8, size=(T, k)) / 8.0).astype(np.float32)
-    out = moe.moe_combine(to_dev(inputs.f32_to_bf16_bits(y)), to_dev(w), to_dev(inv), True)
-    ref = orc.combine(y[:S].astype(np.float64), inv, w.astype(np.float64), y[S:].astype(np.float64))
+    out = moe.moe_combine(to_dev(inputs.f32_to_bf16_bits(y)), to_dev(w), to_dev(inv), ys=to_dev(ys))
+    ref = orc.combine(y.astype(np.float64), inv, w.astype(np.float64), ys.astype(np.float64))
     assert (bf16_bits(out) == inputs.f32_to_bf16_bits(ref.astype(np.float32))).all()
 
 
@@ -208,7 +220,7 @@ def test_grouped_gemms_full_size_sampled(moe, name):
     h = moe.moe_grouped_swiglu(to_dev(xs_bits), offs, to_dev(L["W1"]), to_dev(L["W3"]), T, k,
                                x=to_dev(L["x"]) if w_.shared else None,
                                Ws1=to_dev(L["Ws1"]), Ws3=to_dev(L["Ws3"]))
-    y = moe.moe_grouped_down(h, offs, to_dev(L["W2"]), T, k, Ws2=to_dev(L["Ws2"]))
+    y, _ = moe.moe_grouped_down(h, offs, to_dev(L["W2"]), T, k, Ws2=to_dev(L["Ws2"]))
     torch.cuda.synchronize()
     S = T * k
     rng = np.random.default_rng(0)

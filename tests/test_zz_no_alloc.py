@@ -80,9 +80,32 @@ def test_noalloc_matches_scratch_entry_on_two_calls_in_a_row(native):
         assert torch.equal(got["x_sorted"].view(torch.int16), ref["x_sorted"].view(torch.int16))
 
 
+def test_noalloc_at_the_size_limit(native):
+    """With 16-token histogram blocks, T = 8192 and E = 128 need exactly the
+    65,536 entries the array holds: accepted, and equal to moe_permute.  Sixteen
+    more tokens need one more block row: rejected before anything runs."""
+    N = native
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if 32 * 2 * sms <= 8208:
+        pytest.skip("16-token blocks need more SMs than this device has at T = 8208")
+    E, k = 128, 1
+    need = lambda T: -(-T // int(N.lib.moe_route_block_tokens(T))) * E
+    assert need(8192) == 65536 and need(8208) == 65536 + E
+    ids, x = _case(8192, E, k, 3)
+    ref = _permute_with_scratch(N, ids, E, x)
+    got = _permute_noalloc(N, ids, E, x)
+    torch.cuda.synchronize()
+    for name in ("counts", "offsets", "perm", "inv"):
+        assert torch.equal(got[name], ref[name]), name
+    assert torch.equal(got["x_sorted"].view(torch.int16), ref["x_sorted"].view(torch.int16))
+    fake = ctypes.c_void_p(0x100000)
+    st = N.lib.moe_permute_noalloc(fake, N.dims(8208, 128, 64, E, k), fake, fake, fake, fake, None, None, None)
+    assert st == N.MOE_ERR_UNSUPPORTED_SHAPE
+
+
 def test_noalloc_rejects_sizes_beyond_its_array(native):
     N = native
-    T, E, k = 65 * 1024, 128, 1          # ceil(T/64) * E = 133,120 > 65,536
+    T, E, k = 65 * 1024, 128, 1          # 64-token blocks: ceil(T/64) * E = 133,120 > 65,536
     fake = ctypes.c_void_p(0x100000)
     st = N.lib.moe_permute_noalloc(fake, N.dims(T, 64, 64, E, k), fake, fake, fake, fake, None, None, None)
     assert st == N.MOE_ERR_UNSUPPORTED_SHAPE
