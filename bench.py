@@ -646,6 +646,25 @@ def main():
     n_launch, wall, KB = tm["launches"], tm["wall_s"], tm["stage_steps"]
     K = args.steps
 
+    # ---- references for the event-timed HBM stages: a plain library read of
+    # the same x (torch's float32 sum over its bytes) and an empty launch,
+    # each after the same L2 flush ----
+    xf = G["x"].view(torch.float32)
+    refs = {"torch_sum_x": lambda: xf.sum(), "empty_launch": lambda: torch.cuda._sleep(0)}
+    ref_ms = {}
+    for name, op in refs.items():
+        fev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(KB)]
+        for _ in range(3):
+            flush_l2()
+            op()
+        for i in range(KB):
+            flush_l2()
+            fev[i][0].record()
+            op()
+            fev[i][1].record()
+        torch.cuda.synchronize()
+        ref_ms[name] = float(np.mean([fev[i][0].elapsed_time(fev[i][1]) for i in range(KB)]))
+
     # ---- the same step replayed from a CUDA graph (the L2 flush stays outside) ----
     gs = torch.cuda.Stream(device=dev)
     gs.wait_stream(torch.cuda.current_stream())
@@ -756,6 +775,10 @@ def main():
         "hbm_stages": {"kernels": "route + permute + combine", "bytes": hbm_bytes, "ms": hbm_stages,
                        "achieved_gbs": hbm_bytes / (hbm_stages / 1e3) / 1e9,
                        "frac": hbm_bytes / (hbm_stages / 1e3) / 1e9 / pk["hbm_gbs"]},
+        "read_reference": {"what": "event-timed after the same L2 flush: torch's float32 sum over x's bytes "
+                                   "(a plain library read of T*D*2 bytes) and an empty kernel launch",
+                           "x_bytes": T * D * 2, "torch_sum_x_ms": ref_ms["torch_sum_x"],
+                           "empty_launch_ms": ref_ms["empty_launch"], "route_stage_ms": st_mean["route"]},
         "e2e": {"value": T * world / (e2e / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 2,
                 "ms_per_step": e2e, "pipelining": f"{nstream} streams, copies overlap compute"},
