@@ -80,8 +80,9 @@ def stage_bytes(w) -> dict:
         "route": T * D * 2 + D * E * 2 + S * 8,
         "permute": T * D * 2 + S * D * 2 + S * 4 * 3,
         "w1w3": S * D * 2 + sh * T * D * 2 + (E + sh) * 2 * D * F * 2 + rows * F * 2,
-        "w2": rows * F * 2 + (E + sh) * F * D * 2 + rows * D * 2,
-        "combine": S * D * 2 + sh * T * D * 2 + T * D * 2 + S * 8,
+        # the shared expert's rows of the down-projection (ys) are fp32
+        "w2": rows * F * 2 + (E + sh) * F * D * 2 + S * D * 2 + sh * T * D * 4,
+        "combine": S * D * 2 + sh * T * D * 4 + T * D * 2 + S * 8,
     }
 
 
