@@ -58,6 +58,7 @@
 //     k-block takes two TMA operations per CTA (A and B) instead of three.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "moe_device.cuh"
@@ -526,6 +527,15 @@ cudaError_t make_weight_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// An upper bound of the pair tiles of one launch, from the shape alone: each
+// of the G groups adds at most one partial 256-row m-tile.  Pairs past it
+// would find no tile, so the grid is capped by it (tiny layers).
+int max_pair_tiles(long rows, int groups, int ntn) {
+  const long mt = (rows + static_cast<long>(groups) * (kPairBM - 1)) / kPairBM;
+  const long t = mt * ntn;
+  return t > (1 << 30) ? (1 << 30) : static_cast<int>(t);
+}
+
 struct DeviceInfo {
   int device = -1;
   int sms = 0;
@@ -674,7 +684,10 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
   if ((e = make_map(&mC, h, static_cast<uint64_t>(S) + (shared ? d.T : 0), d.F, kOutBoxRows, kOutBoxCols)) !=
       cudaSuccess)
     return e;
-  e = launch_pair<true>(di.pair_clusters[1], mA, mAs, mB0, mB1, mB0s, mB1s, mC, mC, a, s, pdl);
+  const int groups1 = d.E + (shared ? 1 : 0);
+  const int pairs1 = std::min(di.pair_clusters[1],
+                              max_pair_tiles(static_cast<long>(S) + (shared ? d.T : 0), groups1, (d.F + hw - 1) / hw));
+  e = launch_pair<true>(pairs1, mA, mAs, mB0, mB1, mB0s, mB1s, mC, mC, a, s, pdl);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -716,7 +729,10 @@ cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uin
   } else {
     mCs = mC;
   }
-  e = launch_pair<false>(di.pair_clusters[0], mA, mA, mB0, mB0, mB0s, mB0s, mC, mCs, a, s, pdl);
+  const int groups0 = d.E + (shared ? 1 : 0);
+  const int pairs0 = std::min(di.pair_clusters[0],
+                              max_pair_tiles(static_cast<long>(S) + (shared ? d.T : 0), groups0, (d.D + tn - 1) / tn));
+  e = launch_pair<false>(pairs0, mA, mA, mB0, mB0, mB0s, mB0s, mC, mCs, a, s, pdl);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -76,21 +76,33 @@ MOE_DEV void mma_m16n8k16_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t
 // irrelevant.  The router weights are packed once per call in the matching
 // fragment order: wpack[chunk][expert tile][lane] = 16 bytes holding
 // Wg[32 chunk + 8c + j][8 tile + g], j = 0..7 (zero for padded experts).
-__global__ void __launch_bounds__(256) pack_router_weights_kernel(const uint16_t* __restrict__ Wg, int D,
-                                                                  int E, int NT, uint4* __restrict__ wpack) {
-  griddep_launch_dependents();
-  const int slot = blockIdx.x * blockDim.x + threadIdx.x;
-  if (slot >= (D / 32) * NT * 32) return;
+// Fragment slot `slot` of the packed router weights from Wg [D, E].
+MOE_DEV uint4 pack_wg_slot(const uint16_t* __restrict__ Wg, int E, int NT, int slot) {
   const int lane = slot & 31, n = (slot >> 5) % NT, kc = (slot >> 5) / NT;
   const int e = 8 * n + (lane >> 2), d0 = 32 * kc + 8 * (lane & 3);
   uint32_t w[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const uint32_t lo = e < E ? Wg[static_cast<size_t>(d0 + 2 * j) * E + e] : 0u;
-    const uint32_t hi = e < E ? Wg[static_cast<size_t>(d0 + 2 * j + 1) * E + e] : 0u;
+    const uint32_t lo = e < E ? __ldg(Wg + static_cast<size_t>(d0 + 2 * j) * E + e) : 0u;
+    const uint32_t hi = e < E ? __ldg(Wg + static_cast<size_t>(d0 + 2 * j + 1) * E + e) : 0u;
     w[j] = lo | (hi << 16);
   }
-  wpack[slot] = make_uint4(w[0], w[1], w[2], w[3]);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Packed router weights up to this size are packed by each router block
+// into its own shared memory (no separate packing launch).
+#ifndef MOE_ROUTE_SELF_PACK_BYTES
+#define MOE_ROUTE_SELF_PACK_BYTES (16 * 1024)
+#endif
+constexpr size_t kRouteSelfPackBytes = MOE_ROUTE_SELF_PACK_BYTES;
+
+__global__ void __launch_bounds__(256) pack_router_weights_kernel(const uint16_t* __restrict__ Wg, int D,
+                                                                  int E, int NT, uint4* __restrict__ wpack) {
+  griddep_launch_dependents();
+  const int slot = blockIdx.x * blockDim.x + threadIdx.x;
+  if (slot >= (D / 32) * NT * 32) return;
+  wpack[slot] = pack_wg_slot(Wg, E, NT, slot);
 }
 
 // Resident blocks per SM the register budget is sized for: all blocks of a
@@ -192,10 +204,11 @@ MOE_DEV void select_topk(const float (&acc)[NT][4], int row0, int row1, int c, i
 // not-yet-chosen logit (ties to the lower expert index) across the quad.
 template <int NT, int KMAX>
 __global__ void __launch_bounds__(kRouteThreads, route_min_blocks(NT)) route_kernel(
-    const uint16_t* __restrict__ x, const uint4* __restrict__ wpack, const float* __restrict__ bias,
-    int T, int D, int E, int k, int TB, int32_t* __restrict__ ids, float* __restrict__ wts,
-    int32_t* __restrict__ hist) {
-  extern __shared__ float red[];  // [8 warps][NT][4][32]: partial logits
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ Wg, const uint4* __restrict__ wpack,
+    int self_pack, const float* __restrict__ bias, int T, int D, int E, int k, int TB,
+    int32_t* __restrict__ ids, float* __restrict__ wts, int32_t* __restrict__ hist) {
+  extern __shared__ float red[];  // [8 warps][NT][4][32]: partial logits, then (self_pack) the packed weights
+  uint4* wps = reinterpret_cast<uint4*>(red + 8 * NT * 4 * 32);
   __shared__ int s_hist[MOE_MAX_EXPERTS];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -228,10 +241,17 @@ __global__ void __launch_bounds__(kRouteThreads, route_min_blocks(NT)) route_ker
     }
   };
   // x does not come from the previous kernel (the weight packing): start
-  // streaming it before waiting for the packed weights
+  // streaming it before waiting for the packed weights (or packing them here
+  // from Wg, an input of the call)
   load_x(split);
+  if (self_pack) {
+    const int nslots = (D / 32) * NT * 32;
+    for (int i = threadIdx.x; i < nslots; i += kRouteThreads) wps[i] = pack_wg_slot(Wg, E, NT, i);
+    __syncthreads();
+  }
   griddep_wait();
   griddep_launch_dependents();
+  const uint4* bsrc = self_pack ? wps : wpack;  // this block's copy, or the packing kernel's
   for (int kc0 = split; kc0 < nkc; kc0 += KG * DS) {
     if (kc0 != split) load_x(kc0);
     uint4 b[KG][NT];
@@ -240,8 +260,9 @@ __global__ void __launch_bounds__(kRouteThreads, route_min_blocks(NT)) route_ker
       const int kc = kc0 + j * DS;
       const bool in = kc < nkc;
 #pragma unroll
-      for (int n = 0; n < NT; ++n)
-        b[j][n] = in ? __ldg(wpack + (static_cast<size_t>(kc) * NT + n) * 32 + lane) : make_uint4(0, 0, 0, 0);
+      for (int n = 0; n < NT; ++n) {
+        b[j][n] = in ? bsrc[(static_cast<size_t>(kc) * NT + n) * 32 + lane] : make_uint4(0, 0, 0, 0);
+      }
     }
 #pragma unroll
     for (int j = 0; j < KG; ++j) {
@@ -504,12 +525,13 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
 }
 
 template <int NT, int KMAX>
-static cudaError_t launch_route_nt(const uint16_t* x, const uint4* wpack, const float* bias,
-                                  const moe_dims& d, int32_t* ids, float* w, int32_t* hist,
-                                  cudaStream_t s, bool pdl) {
+static cudaError_t launch_route_nt(const uint16_t* x, const uint16_t* Wg, const uint4* wpack, bool self_pack,
+                                   const float* bias, const moe_dims& d, int32_t* ids, float* w, int32_t* hist,
+                                   cudaStream_t s, bool pdl) {
   const int TB = route_block_tokens(d.T);
-  constexpr size_t smem = static_cast<size_t>(8) * NT * 4 * 32 * sizeof(float);
-  if (smem > 48 * 1024) {
+  constexpr size_t red_bytes = static_cast<size_t>(8) * NT * 4 * 32 * sizeof(float);
+  const size_t smem = red_bytes + (self_pack ? route_packed_bytes(d.D, d.E) : 0);
+  if (red_bytes + kRouteSelfPackBytes > 48 * 1024) {
     static bool attr_done[64] = {false};
     static std::mutex mu;
     int dev = 0;
@@ -517,25 +539,24 @@ static cudaError_t launch_route_nt(const uint16_t* x, const uint4* wpack, const 
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (!attr_done[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(route_kernel<NT, KMAX>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      cudaError_t e = cudaFuncSetAttribute(route_kernel<NT, KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(red_bytes + kRouteSelfPackBytes));
       if (e != cudaSuccess) return e;
       attr_done[dev] = true;
     }
   }
   return launch_kernel(route_kernel<NT, KMAX>, dim3(route_blocks(d.T)), dim3(kRouteThreads), smem, s, pdl, x,
-                       wpack, bias, d.T, d.D, d.E, d.k, TB, ids, w, hist);
+                       Wg, wpack, self_pack ? 1 : 0, bias, d.T, d.D, d.E, d.k, TB, ids, w, hist);
 }
 
 template <int NT>
-static cudaError_t launch_route_k(const uint16_t* x, const uint4* wpack, const float* bias,
-                                 const moe_dims& d, int32_t* ids, float* w, int32_t* hist,
-                                 cudaStream_t s) {
-  // the router follows the weight-packing kernel of the same call
-  if (d.k <= 2) return launch_route_nt<NT, 2>(x, wpack, bias, d, ids, w, hist, s, true);
-  if (d.k <= 4) return launch_route_nt<NT, 4>(x, wpack, bias, d, ids, w, hist, s, true);
-  if (d.k <= 8) return launch_route_nt<NT, 8>(x, wpack, bias, d, ids, w, hist, s, true);
-  return launch_route_nt<NT, 16>(x, wpack, bias, d, ids, w, hist, s, true);
+static cudaError_t launch_route_k(const uint16_t* x, const uint16_t* Wg, const uint4* wpack, bool self_pack,
+                                  const float* bias, const moe_dims& d, int32_t* ids, float* w, int32_t* hist,
+                                  cudaStream_t s, bool pdl) {
+  if (d.k <= 2) return launch_route_nt<NT, 2>(x, Wg, wpack, self_pack, bias, d, ids, w, hist, s, pdl);
+  if (d.k <= 4) return launch_route_nt<NT, 4>(x, Wg, wpack, self_pack, bias, d, ids, w, hist, s, pdl);
+  if (d.k <= 8) return launch_route_nt<NT, 8>(x, Wg, wpack, self_pack, bias, d, ids, w, hist, s, pdl);
+  return launch_route_nt<NT, 16>(x, Wg, wpack, self_pack, bias, d, ids, w, hist, s, pdl);
 }
 
 cudaError_t launch_route(const uint16_t* x, const uint16_t* Wg, const float* bias, const moe_dims& d,
@@ -543,16 +564,22 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* Wg, const float* bia
                          bool pdl) {
   const int NT = route_expert_tiles(d.E);
   uint4* wpack = static_cast<uint4*>(wpack_buf);
-  const int nslots = (d.D / 32) * NT * 32;
-  cudaError_t e = launch_kernel(pack_router_weights_kernel, dim3((nslots + 255) / 256), dim3(256), 0, s, pdl,
-                                Wg, d.D, d.E, NT, wpack);
-  if (e != cudaSuccess) return e;
+  // Small packed weights: every router block packs its own copy (one launch).
+  // Otherwise a packing kernel writes them once and the router follows it.
+  const bool self_pack = route_packed_bytes(d.D, d.E) <= kRouteSelfPackBytes;
+  if (!self_pack) {
+    const int nslots = (d.D / 32) * NT * 32;
+    cudaError_t e = launch_kernel(pack_router_weights_kernel, dim3((nslots + 255) / 256), dim3(256), 0, s, pdl,
+                                  Wg, d.D, d.E, NT, wpack);
+    if (e != cudaSuccess) return e;
+    pdl = true;
+  }
   switch (NT) {
-    case 1: return launch_route_k<1>(x, wpack, bias, d, ids, w, hist, s);
-    case 2: return launch_route_k<2>(x, wpack, bias, d, ids, w, hist, s);
-    case 4: return launch_route_k<4>(x, wpack, bias, d, ids, w, hist, s);
-    case 8: return launch_route_k<8>(x, wpack, bias, d, ids, w, hist, s);
-    default: return launch_route_k<16>(x, wpack, bias, d, ids, w, hist, s);
+    case 1: return launch_route_k<1>(x, Wg, wpack, self_pack, bias, d, ids, w, hist, s, pdl);
+    case 2: return launch_route_k<2>(x, Wg, wpack, self_pack, bias, d, ids, w, hist, s, pdl);
+    case 4: return launch_route_k<4>(x, Wg, wpack, self_pack, bias, d, ids, w, hist, s, pdl);
+    case 8: return launch_route_k<8>(x, Wg, wpack, self_pack, bias, d, ids, w, hist, s, pdl);
+    default: return launch_route_k<16>(x, Wg, wpack, self_pack, bias, d, ids, w, hist, s, pdl);
   }
 }
 
