@@ -592,9 +592,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = i & 1;
       const uint32_t tph = (i >> 1) & 1;
       // the activation mode's h_bar rows do not depend on this kernel: load
-      // them before waiting for the accumulator
+      // them before waiting for the accumulator, and ask L2 for the next
+      // tile's rows now, so that its loads do not wait a full HBM round trip
       uint32_t hbp[2][16];
       if (kMode == kActBwd) {
+        const int nt = next_tile(i + 1);
+        if (nt >= 0) {
+          int pos2 = pos;
+          while (nt >= ctl.tile_prefix[pos2 + 1]) ++pos2;
+          const int g2 = ctl.gorder[pos2];
+          const TileInfo t2 = tile_info(g2, nt - ctl.tile_prefix[pos2]);
+          const int row2 = t2.m * kTileM + r_in_tile;
+          if (row2 < ctl.pnrows[g2]) {
+            const size_t orow2 = static_cast<size_t>(ctl.prow0[g2] + row2);
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+              const int col = t2.n * hw + part * (hw / 2) + 32 * c2;
+              if (col < p.N) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.hbar + orow2 * p.N + col) : "memory");
+            }
+          }
+        }
         const int row = m * kTileM + r_in_tile;
         if (row < ctl.pnrows[g]) {
           const size_t orow = static_cast<size_t>(ctl.prow0[g] + row);

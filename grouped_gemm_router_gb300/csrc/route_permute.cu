@@ -92,10 +92,7 @@ MOE_DEV uint4 pack_wg_slot(const uint16_t* __restrict__ Wg, int E, int NT, int s
 
 // Packed router weights up to this size are packed by each router block
 // into its own shared memory (no separate packing launch).
-#ifndef MOE_ROUTE_SELF_PACK_BYTES
-#define MOE_ROUTE_SELF_PACK_BYTES (16 * 1024)
-#endif
-constexpr size_t kRouteSelfPackBytes = MOE_ROUTE_SELF_PACK_BYTES;
+constexpr size_t kRouteSelfPackBytes = 16 * 1024;
 
 __global__ void __launch_bounds__(256) pack_router_weights_kernel(const uint16_t* __restrict__ Wg, int D,
                                                                   int E, int NT, uint4* __restrict__ wpack) {
