@@ -73,10 +73,12 @@ MOE_DEV void mma_m16n8k16_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t
 // The router's x loads put, for lane (g = lane / 4, c = lane % 4), columns
 // d + 8c .. d + 8c + 7 of each 32-wide chunk into the MMA k-slots (2c, 2c+1,
 // 2c+8, 2c+9) of two m16n8k16 MMAs; the order of terms in the sum over d is
-// irrelevant.  The router weights are packed once per call in the matching
-// fragment order: wpack[chunk][expert tile][lane] = 16 bytes holding
+// irrelevant.  The router weights are read in the matching fragment order:
+// wpack[chunk][expert tile][lane] = 16 bytes holding
 // Wg[32 chunk + 8c + j][8 tile + g], j = 0..7 (zero for padded experts).
-// Fragment slot `slot` of the packed router weights from Wg [D, E].
+// pack_wg_slot builds one such slot from Wg [D, E]; small packed weights are
+// built by every router block in its shared memory, larger ones once per call
+// by pack_router_weights_kernel.
 MOE_DEV uint4 pack_wg_slot(const uint16_t* __restrict__ Wg, int E, int NT, int slot) {
   const int lane = slot & 31, n = (slot >> 5) % NT, kc = (slot >> 5) / NT;
   const int e = 8 * n + (lane >> 2), d0 = 32 * kc + 8 * (lane & 3);
