@@ -619,6 +619,15 @@ cudaError_t tensor_map_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64
   return make_map(m, ptr, rows, cols, box_rows, box_cols);
 }
 
+cudaError_t tensor_map_blocks(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t nblk) {
+  {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
+  }
+  return make_weight_map(m, ptr, rows, cols, nblk);
+}
+
 cudaError_t tensor_map_f32_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
                               uint32_t box0, uint32_t box1) {
   {

@@ -484,8 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const CUtensorMap* mB =
                   leader ? (routed ? &mapB0 : &mapB0_sh) : (routed ? &mapB1 : &mapB1_sh);
               const int brow = (routed ? g * p.K : 0) + kb * kBK;
-              for (int c = 0; c < half_n / 64; ++c)
-                tma_load_2d_pair(sb + c * 8192, mB, full_leader, n * hw + c * 64, brow, pol_b);
+              tma_load_3d_pair(sb, mB, full_leader, 0, brow, (n * hw) / 64, pol_b);
             } else {
               // B^T rows of this CTA's half of the tile's columns, K-major
               const bool second = kMode == kDgradX && kb * kBK >= p.K1;
@@ -499,12 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ak0 = routed ? (p.a_padded ? ctl.prow0[g] : ctl.row0[g]) : 0;
             const int bk0 = routed ? ctl.prow0[g] : 0;
             const int mcol = m * kTileM + 128 * static_cast<int>(rank);
-            for (int c = 0; c < 2; ++c)
-              tma_load_2d_pair(sa + c * 8192, mA, full_leader, mcol + c * 64, ak0 + kb * kBK, pol_a);
             const CUtensorMap* mB = routed ? &mapB0 : &mapB0_sh;
             const int ncol = n * kTileN + half_n * static_cast<int>(rank);
-            for (int c = 0; c < half_n / 64; ++c)
-              tma_load_2d_pair(sb + c * 8192, mB, full_leader, ncol + c * 64, bk0 + kb * kBK, pol_b);
+            tma_load_3d_pair(sa, mA, full_leader, 0, ak0 + kb * kBK, mcol / 64, pol_a);
+            tma_load_3d_pair(sb, mB, full_leader, 0, bk0 + kb * kBK, ncol / 64, pol_b);
           }
           ++issued;
           if (++stage == kSt) {
@@ -1005,12 +1002,12 @@ cudaError_t launch_bwd_act(const BwdLayout& L, const int32_t* offsets, const uin
   CUtensorMap m[kMaps];
   cudaError_t e;
   if ((e = tensor_map_2d(&m[0], x_sorted, S, d.D, 128, kBK)) != cudaSuccess) return e;
-  if ((e = tensor_map_2d(&m[2], W1, static_cast<uint64_t>(d.E) * d.D, d.F, kBK, 64)) != cudaSuccess) return e;
-  if ((e = tensor_map_2d(&m[3], W3, static_cast<uint64_t>(d.E) * d.D, d.F, kBK, 64)) != cudaSuccess) return e;
+  if ((e = tensor_map_blocks(&m[2], W1, static_cast<uint64_t>(d.E) * d.D, d.F, 2)) != cudaSuccess) return e;
+  if ((e = tensor_map_blocks(&m[3], W3, static_cast<uint64_t>(d.E) * d.D, d.F, 2)) != cudaSuccess) return e;
   if (L.shared) {
     if ((e = tensor_map_2d(&m[1], x, d.T, d.D, 128, kBK)) != cudaSuccess) return e;
-    if ((e = tensor_map_2d(&m[4], Ws1, d.D, d.F, kBK, 64)) != cudaSuccess) return e;
-    if ((e = tensor_map_2d(&m[5], Ws3, d.D, d.F, kBK, 64)) != cudaSuccess) return e;
+    if ((e = tensor_map_blocks(&m[4], Ws1, d.D, d.F, 2)) != cudaSuccess) return e;
+    if ((e = tensor_map_blocks(&m[5], Ws3, d.D, d.F, 2)) != cudaSuccess) return e;
   } else {
     m[1] = m[0];
     m[4] = m[2];
@@ -1073,11 +1070,11 @@ cudaError_t launch_bwd_wgrad(const BwdLayout& L, const int32_t* offsets, const u
   const int S = d.T * d.k;
   CUtensorMap m[kMaps];
   cudaError_t e;
-  if ((e = tensor_map_2d(&m[0], A, a_padded ? L.S_pad : S, M, kBK, 64)) != cudaSuccess) return e;
-  if ((e = tensor_map_2d(&m[2], B, L.S_pad, N, kBK, 64)) != cudaSuccess) return e;
+  if ((e = tensor_map_blocks(&m[0], A, a_padded ? L.S_pad : S, M, 2)) != cudaSuccess) return e;
+  if ((e = tensor_map_blocks(&m[2], B, L.S_pad, N, 2)) != cudaSuccess) return e;
   if (L.shared) {
-    if ((e = tensor_map_2d(&m[1], A_sh, d.T, M, kBK, 64)) != cudaSuccess) return e;
-    if ((e = tensor_map_2d(&m[4], B_sh, d.T, N, kBK, 64)) != cudaSuccess) return e;
+    if ((e = tensor_map_blocks(&m[1], A_sh, d.T, M, 2)) != cudaSuccess) return e;
+    if ((e = tensor_map_blocks(&m[4], B_sh, d.T, N, 2)) != cudaSuccess) return e;
   } else {
     m[1] = m[0];
     m[4] = m[2];
