@@ -72,8 +72,9 @@ constexpr int kMaxMyTiles = 64;
 // into near-equal chunks whose fp32 partial sums a reduction kernel adds.
 constexpr int kMaxChunkKb = 160;
 
-// The activation mode stages three output boxes per epilogue warp (g_bar,
-// u_bar, h) and gives up one stage of the ring for them.
+// The activation mode gives each epilogue warp three output staging buffers
+// (g_bar, u_bar and h boxes rotate through them) and gives up one stage of
+// the ring for them.
 __host__ __device__ constexpr int stages_of(int mode) { return mode == kActBwd ? kStages - 1 : kStages; }
 __host__ __device__ constexpr int out_boxes_of(int mode) { return mode == kActBwd ? 3 : 1; }
 __host__ __device__ constexpr int smem_bytes_of(int mode) {
@@ -578,54 +579,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tempty_leader0 = map_to_cta(smem_u32(&ctl.tempty[0]), 0);
     const uint32_t tempty_leader1 = map_to_cta(smem_u32(&ctl.tempty[1]), 0);
     uint8_t* stage_out = smem + kSt * kStageBytes + (warp - 2) * out_boxes_of(kMode) * kOutBoxBytes;
-    int pos = 0, i = 0;
-    for (int tile = next_tile(0); tile >= 0; tile = next_tile(++i)) {
-      while (tile >= ctl.tile_prefix[pos + 1]) ++pos;
-      const int g = ctl.gorder[pos];
-      const int local = tile - ctl.tile_prefix[pos];
-      const TileInfo ti = tile_info(g, local);
-      const int m = ti.m, n = ti.n;
-      const bool routed = g < p.E;
-      const int buf = i & 1;
-      const uint32_t tph = (i >> 1) & 1;
-      // the activation mode's h_bar rows do not depend on this kernel: load
-      // them before waiting for the accumulator, and ask L2 for the next
-      // tile's rows now, so that its loads do not wait a full HBM round trip
-      uint32_t hbp[2][16];
-      if (kMode == kActBwd) {
+    if constexpr (kMode == kActBwd) {
+      // SwiGLU backward: per tile, warp (q, part) holds rows q*32 .. +31 of
+      // this CTA and two 32-column boxes of g | u.  The h_bar rows it needs do
+      // not depend on this kernel, so they are loaded a box ahead: box 1's
+      // at the start of a tile, the next tile's box 0 right after box 0's
+      // math (its registers are free by then), each a half-tile before use;
+      // L2 is asked for the next tile's rows at the start of a tile.  The
+      // output boxes rotate through the warp's three staging buffers, one
+      // bulk group per box store, so a box waits only for the store issued
+      // two boxes earlier to have read its buffer (g_bar and u_bar), or for
+      // all of them when h is stored too.
+      auto hbar_src = [&](int g_, int m_, int n_, int c) -> const uint16_t* {
+        const int row = m_ * kTileM + r_in_tile;
+        const int col = n_ * hw + part * (hw / 2) + 32 * c;
+        if (row >= ctl.pnrows[g_] || col >= p.N) return nullptr;
+        return p.hbar + static_cast<size_t>(ctl.prow0[g_] + row) * p.N + col;
+      };
+      int pos = 0, i = 0;
+      int tile = next_tile(0);
+      int g = 0, m = 0, n = 0;
+      if (tile >= 0) {
+        while (tile >= ctl.tile_prefix[pos + 1]) ++pos;
+        g = ctl.gorder[pos];
+        const TileInfo ti = tile_info(g, tile - ctl.tile_prefix[pos]);
+        m = ti.m;
+        n = ti.n;
+      }
+      uint32_t hb0[16], hb1[16];
+      if (tile >= 0) {
+        const uint16_t* src = hbar_src(g, m, n, 0);
+        if (src != nullptr) load_bf16x32(src, hb0);
+      }
+      int ring = 0;  // staging buffer of the next output box
+      for (; tile >= 0; ++i) {
         const int nt = next_tile(i + 1);
+        int pos2 = pos, g2 = 0, m2 = 0, n2 = 0;
         if (nt >= 0) {
-          int pos2 = pos;
           while (nt >= ctl.tile_prefix[pos2 + 1]) ++pos2;
-          const int g2 = ctl.gorder[pos2];
+          g2 = ctl.gorder[pos2];
           const TileInfo t2 = tile_info(g2, nt - ctl.tile_prefix[pos2]);
-          const int row2 = t2.m * kTileM + r_in_tile;
-          if (row2 < ctl.pnrows[g2]) {
-            const size_t orow2 = static_cast<size_t>(ctl.prow0[g2] + row2);
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-              const int col = t2.n * hw + part * (hw / 2) + 32 * c2;
-              if (col < p.N) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.hbar + orow2 * p.N + col) : "memory");
-            }
-          }
-        }
-        const int row = m * kTileM + r_in_tile;
-        if (row < ctl.pnrows[g]) {
-          const size_t orow = static_cast<size_t>(ctl.prow0[g] + row);
+          m2 = t2.m;
+          n2 = t2.n;
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
-            const int col = n * hw + part * (hw / 2) + 32 * c2;
-            if (col < p.N) load_bf16x32(p.hbar + orow * p.N + col, hbp[c2]);
+            const uint16_t* src = hbar_src(g2, m2, n2, c2);
+            if (src != nullptr) asm volatile("prefetch.global.L2 [%0];" ::"l"(src) : "memory");
           }
         }
-      }
-      const bool got = mbar_wait_cluster(smem_u32(&ctl.tfull[buf]), tph, abort_flag, dev_err);
-      if (!__all_sync(0xffffffffu, got)) break;
-      tc_fence_after_sync();
-      bool act_released = false;  // kActBwd: accumulator already handed back
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * 256;
-      const int cols_per_part = hw / 2;
-      if (Tr::row_tiles) {
+        {
+          const uint16_t* src = hbar_src(g, m, n, 1);
+          if (src != nullptr) load_bf16x32(src, hb1);
+        }
+        const int buf = i & 1;
+        const uint32_t tph = (i >> 1) & 1;
+        const bool got = mbar_wait_cluster(smem_u32(&ctl.tfull[buf]), tph, abort_flag, dev_err);
+        if (!__all_sync(0xffffffffu, got)) break;
+        tc_fence_after_sync();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * 256;
         const int nvalid = ctl.pnrows[g];
         const int orow0 = ctl.prow0[g];  // output rows (padded layout / shared rows)
         const int row = m * kTileM + r_in_tile;
@@ -633,97 +644,152 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int warp_row0 = m * kTileM + 128 * static_cast<int>(rank) + q * 32;
         const bool full_box = warp_row0 + kOutBoxRows <= nvalid;
         const int col0 = n * hw;
-        constexpr int kChunks = (kMode == kActBwd ? kTileN / 2 : kTileN) / 2 / kOutBoxCols;
-        // The plain-output modes read all of this warp's accumulator columns
-        // in one burst with a single wait and hand the accumulator back
-        // before packing and storing (a wait after every 32-column box holds
-        // the MMAs back).  The SwiGLU-backward mode keeps its h_bar rows in
-        // registers too and reads its two g|u boxes one at a time.
-        uint32_t acc[kMode == kActBwd ? 1 : kChunks][32];
-        if (kMode != kActBwd) {
+        const size_t orow = static_cast<size_t>(orow0 + (valid ? row : 0));
+        bool released = false, next0 = false;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int cc = part * (hw / 2) + c2 * kOutBoxCols;
+          if (col0 + cc >= p.N) break;
+          uint32_t rg[32], ru[32];
+          tmem_ld_32cols(taddr + cc, rg);
+          tmem_ld_32cols(taddr + hw + cc, ru);
+          tmem_ld_wait();
+          if (c2 == 1 || col0 + cc + kOutBoxCols >= p.N) {
+            // the last box is in registers: hand the accumulator back
+            // before its math and stores
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
+            released = true;
+          }
+          const uint32_t(&hb)[16] = c2 == 0 ? hb0 : hb1;
+          uint8_t* sg = stage_out + ring * kOutBoxBytes;
+          uint8_t* su = stage_out + (ring == 2 ? 0 : ring + 1) * kOutBoxBytes;
+          uint8_t* sh = stage_out + (ring == 0 ? 2 : ring - 1) * kOutBoxBytes;
+          if (full_box) {
+            // the stores that last read these buffers are done reading
+            if (want_h)
+              bulk_wait_group_read0();
+            else
+              bulk_wait_group_read1();
+            __syncwarp();
+          }
+          // 16-byte chunk v of the row: columns 8 v .. 8 v + 7 of the box
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t og[4], ou[4], oh[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int j = 4 * v + jj;
+              float gb[2], ub[2], hv[2];
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                const float gg = __uint_as_float(rg[2 * j + t]);
+                const float uu = __uint_as_float(ru[2 * j + t]);
+                const float hh = t ? bf16_hi(hb[j]) : bf16_lo(hb[j]);
+                const float e = __expf(-gg);
+                const float sig = __fdividef(1.0f, 1.0f + e);
+                const float silu = __fdividef(gg, 1.0f + e);  // the forward's expression
+                hv[t] = silu * uu;
+                // silu'(g) = sigmoid(g) (1 + g (1 - sigmoid(g)))
+                gb[t] = hh * uu * (sig * (1.0f + gg * (1.0f - sig)));
+                ub[t] = hh * silu;
+              }
+              og[jj] = pack_bf16x2(gb[0], gb[1]);
+              ou[jj] = pack_bf16x2(ub[0], ub[1]);
+              oh[jj] = pack_bf16x2(hv[0], hv[1]);
+            }
+            if (full_box) {
+              const int sw = lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4);
+              *reinterpret_cast<uint4*>(sg + sw) = make_uint4(og[0], og[1], og[2], og[3]);
+              *reinterpret_cast<uint4*>(su + sw) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+              if (want_h) *reinterpret_cast<uint4*>(sh + sw) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+            } else if (valid) {
+              uint16_t* gdst = p.gu + orow * (2 * p.N) + col0 + cc + 8 * v;
+              *reinterpret_cast<uint4*>(gdst) = make_uint4(og[0], og[1], og[2], og[3]);
+              *reinterpret_cast<uint4*>(gdst + p.N) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+              if (want_h)
+                *reinterpret_cast<uint4*>(p.h + orow * p.N + col0 + cc + 8 * v) =
+                    make_uint4(oh[0], oh[1], oh[2], oh[3]);
+            }
+          }
+          if (full_box) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int r0 = orow0 + warp_row0;
+              tma_store_2d(&mapC, smem_u32(sg), col0 + cc, r0);
+              bulk_commit_group();
+              tma_store_2d(&mapC, smem_u32(su), p.N + col0 + cc, r0);
+              bulk_commit_group();
+              if (want_h) {
+                tma_store_2d(&mapC2, smem_u32(sh), col0 + cc, r0);
+                bulk_commit_group();
+              }
+            }
+            ring = want_h ? ring : (ring == 0 ? 2 : ring - 1);
+          }
+          if (c2 == 0 && nt >= 0) {
+            // box 0's h_bar registers are free: the next tile's box 0 rows
+            const uint16_t* src = hbar_src(g2, m2, n2, 0);
+            if (src != nullptr) load_bf16x32(src, hb0);
+            next0 = true;
+          }
+        }
+        if (!next0 && nt >= 0) {  // this warp had no box in this tile
+          const uint16_t* src = hbar_src(g2, m2, n2, 0);
+          if (src != nullptr) load_bf16x32(src, hb0);
+        }
+        if (!released) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
+        }
+        tile = nt;
+        pos = pos2;
+        g = g2;
+        m = m2;
+        n = n2;
+      }
+    } else {
+      int pos = 0, i = 0;
+      for (int tile = next_tile(0); tile >= 0; tile = next_tile(++i)) {
+        while (tile >= ctl.tile_prefix[pos + 1]) ++pos;
+        const int g = ctl.gorder[pos];
+        const int local = tile - ctl.tile_prefix[pos];
+        const TileInfo ti = tile_info(g, local);
+        const int m = ti.m, n = ti.n;
+        const bool routed = g < p.E;
+        const int buf = i & 1;
+        const uint32_t tph = (i >> 1) & 1;
+        const bool got = mbar_wait_cluster(smem_u32(&ctl.tfull[buf]), tph, abort_flag, dev_err);
+        if (!__all_sync(0xffffffffu, got)) break;
+        tc_fence_after_sync();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * 256;
+        const int cols_per_part = hw / 2;
+        if (Tr::row_tiles) {
+          const int nvalid = ctl.pnrows[g];
+          const int orow0 = ctl.prow0[g];  // output rows (padded layout / shared rows)
+          const int row = m * kTileM + r_in_tile;
+          const bool valid = row < nvalid;
+          const int warp_row0 = m * kTileM + 128 * static_cast<int>(rank) + q * 32;
+          const bool full_box = warp_row0 + kOutBoxRows <= nvalid;
+          const int col0 = n * hw;
+          constexpr int kChunks = kTileN / 2 / kOutBoxCols;
+          // All of this warp's accumulator columns are read in one burst with a
+          // single wait, and the accumulator is handed back before packing and
+          // storing (a wait after every 32-column box holds the MMAs back).
+          uint32_t acc[kChunks][32];
 #pragma unroll
           for (int c2 = 0; c2 < kChunks; ++c2) tmem_ld_32cols(taddr + part * cols_per_part + c2 * kOutBoxCols, acc[c2]);
           tmem_ld_wait();
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
-        }
 #pragma unroll
-        for (int c2 = 0; c2 < kChunks; ++c2) {
-          const int cc = part * cols_per_part + c2 * kOutBoxCols;
-          if (col0 + cc >= p.N) break;
-          if (kMode == kActBwd) {
-            uint32_t rg[32], ru[32];
-            tmem_ld_32cols(taddr + cc, rg);
-            tmem_ld_32cols(taddr + hw + cc, ru);
-            tmem_ld_wait();
-            if (c2 == kChunks - 1 || col0 + cc + kOutBoxCols >= p.N) {
-              // the last box is in registers: hand the accumulator back
-              // before its math and stores
-              tc_fence_before_sync();
-              __syncwarp();
-              if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
-              act_released = true;
-            }
-            const uint32_t(&hb)[16] = hbp[c2 < 2 ? c2 : 1];
-            if (full_box) {
-              bulk_wait_group_read0();  // the previous chunk's stores have read the buffers
-              __syncwarp();
-            }
-            const size_t orow = static_cast<size_t>(orow0 + (valid ? row : 0));
-            // 16-byte chunk v of the row: columns 8 v .. 8 v + 7 of the box
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t og[4], ou[4], oh[4];
-#pragma unroll
-              for (int jj = 0; jj < 4; ++jj) {
-                const int j = 4 * v + jj;
-                float gb[2], ub[2], hv[2];
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                  const float gg = __uint_as_float(rg[2 * j + t]);
-                  const float uu = __uint_as_float(ru[2 * j + t]);
-                  const float hh = t ? bf16_hi(hb[j]) : bf16_lo(hb[j]);
-                  const float e = __expf(-gg);
-                  const float sig = __fdividef(1.0f, 1.0f + e);
-                  const float silu = __fdividef(gg, 1.0f + e);  // the forward's expression
-                  hv[t] = silu * uu;
-                  // silu'(g) = sigmoid(g) (1 + g (1 - sigmoid(g)))
-                  gb[t] = hh * uu * (sig * (1.0f + gg * (1.0f - sig)));
-                  ub[t] = hh * silu;
-                }
-                og[jj] = pack_bf16x2(gb[0], gb[1]);
-                ou[jj] = pack_bf16x2(ub[0], ub[1]);
-                oh[jj] = pack_bf16x2(hv[0], hv[1]);
-              }
-              if (full_box) {
-                const int sw = lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4);
-                *reinterpret_cast<uint4*>(stage_out + sw) = make_uint4(og[0], og[1], og[2], og[3]);
-                *reinterpret_cast<uint4*>(stage_out + kOutBoxBytes + sw) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
-                if (want_h)
-                  *reinterpret_cast<uint4*>(stage_out + 2 * kOutBoxBytes + sw) =
-                      make_uint4(oh[0], oh[1], oh[2], oh[3]);
-              } else if (valid) {
-                uint16_t* gdst = p.gu + orow * (2 * p.N) + col0 + cc + 8 * v;
-                *reinterpret_cast<uint4*>(gdst) = make_uint4(og[0], og[1], og[2], og[3]);
-                *reinterpret_cast<uint4*>(gdst + p.N) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
-                if (want_h)
-                  *reinterpret_cast<uint4*>(p.h + orow * p.N + col0 + cc + 8 * v) =
-                      make_uint4(oh[0], oh[1], oh[2], oh[3]);
-              }
-            }
-            if (full_box) {
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) {
-                const int r0 = orow0 + warp_row0;
-                tma_store_2d(&mapC, smem_u32(stage_out), col0 + cc, r0);
-                tma_store_2d(&mapC, smem_u32(stage_out + kOutBoxBytes), p.N + col0 + cc, r0);
-                if (want_h) tma_store_2d(&mapC2, smem_u32(stage_out + 2 * kOutBoxBytes), col0 + cc, r0);
-                bulk_commit_group();
-              }
-            }
-          } else {
+          for (int c2 = 0; c2 < kChunks; ++c2) {
+            const int cc = part * cols_per_part + c2 * kOutBoxCols;
+            if (col0 + cc >= p.N) break;
             uint32_t packed[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j)
@@ -746,69 +812,64 @@ __global__ void __launch_bounds__(kThreads, 1)
               store_bf16x32(p.C + static_cast<size_t>(orow0 + row) * p.N + col0 + cc, packed);
             }
           }
-        }
-      } else {
-        // kWgrad: fp32 rows m * 256 + r (< M), columns n * 256 + cc (< N);
-        // a split group's chunk goes to its partial slot.  Each 32 x 16 box
-        // is staged with the 64-byte swizzle (conflict-free 16-byte writes)
-        // and written by one TMA store; rows past M are clipped by the map.
-        const bool empty_k = ti.kb1 <= ti.kb0;
-        const bool split = ctl.nchunk[g] > 1;
-        const int warp_row0 = m * kTileM + 128 * static_cast<int>(rank) + q * 32;
-        const bool any_row = warp_row0 < p.M;
-        // all of this warp's columns in one burst, then the accumulator is released
-        constexpr int kBoxes = kTileN / 2 / 32;
-        uint32_t acc[kBoxes][32];
-        if (any_row) {
+        } else {
+          // kWgrad: fp32 rows m * 256 + r (< M), columns n * 256 + cc (< N);
+          // a split group's chunk goes to its partial slot.  Each 32 x 16 box
+          // is staged with the 64-byte swizzle (conflict-free 16-byte writes)
+          // and written by one TMA store; rows past M are clipped by the map.
+          const bool empty_k = ti.kb1 <= ti.kb0;
+          const bool split = ctl.nchunk[g] > 1;
+          const int warp_row0 = m * kTileM + 128 * static_cast<int>(rank) + q * 32;
+          const bool any_row = warp_row0 < p.M;
+          // all of this warp's columns in one burst, then the accumulator is released
+          constexpr int kBoxes = kTileN / 2 / 32;
+          uint32_t acc[kBoxes][32];
+          if (any_row) {
 #pragma unroll
-          for (int b = 0; b < kBoxes; ++b) tmem_ld_32cols(taddr + part * cols_per_part + 32 * b, acc[b]);
-          tmem_ld_wait();
-        }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
-#pragma unroll
-        for (int b = 0; b < kBoxes; ++b) {
-          const int cc = part * cols_per_part + 32 * b;
-          const int col = n * kTileN + cc;
-          if (col >= p.N || !any_row) break;
-          const uint32_t(&ra)[32] = acc[b];
-          const CUtensorMap* om;
-          int x, z;
-          if (split) {
-            om = &mapC5;
-            x = col;
-            z = ctl.pslot[g] + ti.c;
-          } else {
-            const bool second = col >= p.n_split;
-            om = routed ? (second ? &mapC2 : &mapC) : (second ? &mapC4 : &mapC3);
-            x = second ? col - p.n_split : col;
-            z = routed ? g : 0;
+            for (int b = 0; b < kBoxes; ++b) tmem_ld_32cols(taddr + part * cols_per_part + 32 * b, acc[b]);
+            tmem_ld_wait();
           }
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            bulk_wait_group_read0();  // the previous box's store has read the buffer
-            __syncwarp();
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int j = 16 * hh + 4 * v;
-              const uint4 val = empty_k ? make_uint4(0u, 0u, 0u, 0u)
-                                        : make_uint4(ra[j], ra[j + 1], ra[j + 2], ra[j + 3]);
-              *reinterpret_cast<uint4*>(stage_out + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = val;
+          for (int b = 0; b < kBoxes; ++b) {
+            const int cc = part * cols_per_part + 32 * b;
+            const int col = n * kTileN + cc;
+            if (col >= p.N || !any_row) break;
+            const uint32_t(&ra)[32] = acc[b];
+            const CUtensorMap* om;
+            int x, z;
+            if (split) {
+              om = &mapC5;
+              x = col;
+              z = ctl.pslot[g] + ti.c;
+            } else {
+              const bool second = col >= p.n_split;
+              om = routed ? (second ? &mapC2 : &mapC) : (second ? &mapC4 : &mapC3);
+              x = second ? col - p.n_split : col;
+              z = routed ? g : 0;
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_3d(om, smem_u32(stage_out), x + kWOutCols * hh, warp_row0, z);
-              bulk_commit_group();
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              bulk_wait_group_read0();  // the previous box's store has read the buffer
+              __syncwarp();
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const int j = 16 * hh + 4 * v;
+                const uint4 val = empty_k ? make_uint4(0u, 0u, 0u, 0u)
+                                          : make_uint4(ra[j], ra[j + 1], ra[j + 2], ra[j + 3]);
+                *reinterpret_cast<uint4*>(stage_out + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = val;
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(om, smem_u32(stage_out), x + kWOutCols * hh, warp_row0, z);
+                bulk_commit_group();
+              }
             }
           }
         }
-      }
-      if (kMode == kActBwd && !act_released) {
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
       }
     }
     if (lane == 0) bulk_wait_group0();
