@@ -582,6 +582,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=list(inputs.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-streams", type=int, default=4,
+                    help="streams (each with its own workspace) in the end-to-end host-buffer loop")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip timing the other synthetic workloads after the headline one")
     ap.add_argument("--sweep", choices=["fd", "t", "all", "chained"], default=None,
@@ -693,17 +695,22 @@ def main():
     del graph
 
     # ---- end to end through the host-memory entry point ----
-    # Two streams, each with its own workspace and pinned x / out buffers:
-    # while one batch computes, the other's x is copied in and its out copied
-    # back, as a serving loop would run it.  Every step copies its whole x
+    # args.e2e_streams streams, each with its own workspace and pinned x / out
+    # buffers: while one batch computes, the others' x are copied in and their
+    # out copied back, as a serving loop would run it.  A stream's own copies
+    # and layer run in order, so with two streams a stream's D2H and next H2D
+    # (about 0.5 ms together at ~200 GB/s for gptoss_lite) outlast the other
+    # stream's layer; with four the copies hide under the layers (gptoss_lite:
+    # 520, 508 and 496 us per step with two, three and four).  Every step copies its whole x
     # from pinned host memory and its whole out back to pinned host memory
-    # inside the timed region (no L2 flush between these steps).
-    nstream = 2
+    # inside the timed region (no L2 flush between these steps); the region
+    # also holds the pipeline's fill (first H2D) and drain (last D2H).
+    nstream = args.e2e_streams
     streams = [torch.cuda.Stream(device=dev) for _ in range(nstream)]
     ws_h = [moe.Workspace(T, D, F, E, k, w.shared, host_io=True, device=dev) for _ in range(nstream)]
     x_host = [G["x"].cpu().pin_memory() for _ in range(nstream)]
     out_host = [torch.empty(T, D, dtype=torch.bfloat16).pin_memory() for _ in range(nstream)]
-    K2 = max(4, min(K, 50))
+    K2 = max(50, min(K, 200))  # fill and drain spread over at least 50 steps
 
     def e2e_step(i):
         j = i % nstream
@@ -711,7 +718,7 @@ def main():
             moe.moe_ffn_forward_host(x_host[j], G["Wg"], G["W1"], G["W3"], G["W2"], k, out_host[j], ws_h[j],
                                      bias=G["bias"], Ws1=G["Ws1"], Ws3=G["Ws3"], Ws2=G["Ws2"])
 
-    for i in range(args.warmup):
+    for i in range(max(args.warmup, nstream)):
         e2e_step(i)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -725,7 +732,8 @@ def main():
     ev1.record()
     torch.cuda.synchronize()
     e2e = reduce_max(ev0.elapsed_time(ev1) / K2, dev)
-    assert torch.equal(out_host[0], out_host[1])  # both pipelines computed the same layer
+    for j in range(1, nstream):  # every pipeline computed the same layer
+        assert torch.equal(out_host[0], out_host[j])
 
     pk, pk_kind = peaks()
     st_mean = stage_ms
@@ -782,7 +790,7 @@ def main():
                            "empty_launch_ms": ref_ms["empty_launch"], "route_stage_ms": st_mean["route"]},
         "e2e": {"value": T * world / (e2e / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 2,
-                "ms_per_step": e2e, "pipelining": f"{nstream} streams, copies overlap compute"},
+                "ms_per_step": e2e, "steps": K2, "pipelining": f"{nstream} streams, copies overlap compute"},
         "graph": {"ms_per_step": graph_ms, "value": T * world / (graph_ms / 1e3), "unit": "tokens/s",
                   "note": "the same step captured once in a CUDA graph and replayed"},
         "gpu_launches": int(n_launch),
