@@ -34,28 +34,33 @@
 // [r N/2, (r+1) N/2) of the B tile; the leader (r = 0) issues one
 // tcgen05.mma.cta_group::2 per 16-deep k-slice, which writes each CTA's 128
 // rows of D into that CTA's own TMEM.  Per SM, a 128x256 output tile then
-// stages 16 KB of A and 16 KB of B per 64-deep k-block instead of 16 + 32 KB.
+// stages 16 KB of A and 16 KB of B per 64 k instead of 16 + 32 KB.
 //
 // Warp roles (64 + 32 kEpiWarps threads per CTA, one CTA per SM):
 //   warp 0     TMA producer (one lane) -- both CTAs load their own halves
 //   warp 1     TMEM allocator; MMA issuer (one lane, leader only)
 //   warps 2-   epilogue (kEpiWarps): warp w reads TMEM lanes 32 (w % 4) .. + 31
 //              and the columns of part (w - 2) / 4 of the tile
-// Pipelines: kPairStages shared-memory stages (full / empty mbarriers) and
-// two TMEM accumulators of 256 columns (tmem_full / tmem_empty), so the
-// epilogue of one tile overlaps the MMAs of the next.
+// Pipelines: a ring of shared-memory stages (full / empty mbarriers; 3 stages
+// of 128 k for W1||W3, 6 of 64 k for W2, 192 KB either way) and two TMEM
+// accumulators of 256 columns (tmem_full / tmem_empty), so the epilogue of
+// one tile overlaps the MMAs of the next.
 //
-// Shared-memory operand layouts (TMA, 128-byte swizzle):
-//   A tile 128 rows x 64 k (K-major): row r at byte 128 r, 8-row atoms of
-//     1024 bytes -> descriptor SBO = 1024; the k-th 16-wide slice starts
-//     32 k bytes into the tile.
-//   B tile 64 k x N/2 (N-major, straight from the [K, N] row-major weights):
-//     N/2 is split in 64-column blocks of 64 k-rows x 128 bytes (8 KB each);
-//     LBO = 8192 (next 64 columns), SBO = 1024 (next 8 k-rows); the k-th
-//     16-deep slice starts 2048 k bytes into the tile.  One 3-D TMA box
-//     {64 columns, 64 rows, N/128 blocks} over the view {64, K rows, N / 64}
-//     (strides N * 2 and 128 bytes) lands the blocks in that order, so a
-//     k-block takes two TMA operations per CTA (A and B) instead of three.
+// Shared-memory operand layouts (TMA, 128-byte swizzle), per 64 k (one
+// swizzle atom; a 128-deep stage holds two of each, back to back):
+//   A 128 rows x 64 k (K-major): row r at byte 128 r, 8-row atoms of 1024
+//     bytes -> descriptor SBO = 1024; the k-th 16-wide slice starts 32 k
+//     bytes into the atom.  One 3-D TMA box {64, 128 rows, kBK / 64 atoms}
+//     over the view {64, rows, K / 64} (strides K * 2 and 128 bytes) loads a
+//     stage's atoms.
+//   B kBK k x N/2 (N-major, straight from the [K, N] row-major weights): N/2
+//     is split in 64-column blocks of kBK k-rows x 128 bytes; LBO = one block
+//     (next 64 columns), SBO = 1024 (next 8 k-rows); the k-th 16-deep slice
+//     starts 2048 k bytes into a block.  One 3-D TMA box {64 columns, kBK
+//     rows, N/128 blocks} over the view {64, K rows, N / 64} (strides N * 2
+//     and 128 bytes) lands the blocks in that order.
+// A stage thus costs each CTA two TMA operations: per byte, the 128-deep
+// stages of W1||W3 issue half as many as 64-deep ones would.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -68,7 +73,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kBK = 64;                       // k per stage (128 bytes of bf16)
+constexpr int kAtomK = 64;                     // k of one 128-byte swizzle atom (128 bytes of bf16)
 #ifndef MOE_EPI_WARPS
 #define MOE_EPI_WARPS 8
 #endif
@@ -101,10 +106,20 @@ struct GemmArgs {
 // warps of both CTAs.
 // ---------------------------------------------------------------------------
 constexpr int kPairBM = 256;                  // rows per pair tile
-constexpr int kPairStages = 6;
-constexpr int kPairABytes = 128 * kBK * 2;    // 16 KB: this CTA's 128 rows
-constexpr int kPairBBytesMax = 128 * kBK * 2; // 16 KB: this CTA's half of N <= 256
-constexpr int kPairStageBytes = kPairABytes + kPairBBytesMax;
+constexpr int kMaxPairStages = 6;
+// The stage ring of each GEMM: 192 KB per CTA either way.  W1||W3 stages
+// 128-deep k blocks (two swizzle atoms of A and of B, one TMA operation
+// each), W2 64-deep ones: halving the TMA operations per byte took W1||W3
+// from 277 to 258 us on gptoss_lite, while W2, whose A rows come from HBM,
+// ran 146 -> 149 us with three deep stages and keeps six.
+template <bool kSwiGLU>
+struct Ring {
+  static constexpr int kBK = kSwiGLU ? 128 : 64;          // k per stage
+  static constexpr int kStages = kSwiGLU ? 3 : 6;
+  static constexpr int kABytes = 128 * kBK * 2;           // this CTA's 128 rows
+  static constexpr int kBBytesMax = 128 * kBK * 2;        // this CTA's half of N <= 256
+  static constexpr int kStageBytes = kABytes + kBBytesMax;
+};
 constexpr int kOutBoxRows = 32;                 // one epilogue warp's rows
 constexpr int kOutBoxCols = 32;                 // columns per TMA store box (64 bytes)
 constexpr int kOutBoxBytes = kOutBoxRows * kOutBoxCols * 2;
@@ -117,12 +132,14 @@ struct EpiShape {
   static constexpr int kMaxBoxes = (kSwiGLU ? 128 : 256) / kEpiParts / kOutBoxCols;
   static constexpr int kAccRegs = kMaxBoxes * 32 * (kSwiGLU ? 2 : 1);
 };
-constexpr int kPairSmemBytes =
-    kPairStages * kPairStageBytes + kEpiWarps * kOutBufs * kOutBoxBytes + 1024;
+template <bool kSwiGLU>
+constexpr int pair_smem_bytes() {
+  return Ring<kSwiGLU>::kStages * Ring<kSwiGLU>::kStageBytes + kEpiWarps * kOutBufs * kOutBoxBytes + 1024;
+}
 
 struct PairCtl {
-  uint64_t full[kPairStages];
-  uint64_t empty[kPairStages];
+  uint64_t full[kMaxPairStages];
+  uint64_t empty[kMaxPairStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -158,7 +175,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.E + (p.T_shared > 0 ? 1 : 0);
   const int hw = kSwiGLU ? p.tile_n / 2 : p.tile_n;  // output columns per tile
   const int ntn = (p.N + hw - 1) / hw;
-  const int nkb = p.K / kBK;
+  constexpr int kBK = Ring<kSwiGLU>::kBK;
+  constexpr int kPairStages = Ring<kSwiGLU>::kStages;
+  constexpr int kPairABytes = Ring<kSwiGLU>::kABytes;
+  constexpr int kPairStageBytes = Ring<kSwiGLU>::kStageBytes;
+  const int nkb = (p.K + kBK - 1) / kBK;  // a K of 64 mod 128 reads zeros past D (TMA fill)
   const int half_n = p.tile_n / 2;                    // B columns staged by this CTA
   constexpr int kMaxBoxes = EpiShape<kSwiGLU>::kMaxBoxes;
   constexpr int kAccRegs = EpiShape<kSwiGLU>::kAccRegs;
@@ -278,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = smem_base + stage * kPairStageBytes;
           const uint32_t sb = sa + kPairABytes;
           if (leader) mbar_arrive_expect_tx(smem_u32(&ctl.full[stage]), pair_tx);
-          if (load_a) tma_load_2d_pair(sa, mA, full_leader, kb * kBK, a_row, pol_a);
+          if (load_a) tma_load_3d_pair(sa, mA, full_leader, 0, a_row, kb * (kBK / kAtomK), pol_a);
           const int brow = b_row0 + kb * kBK;
           tma_load_3d_pair(sb, mB, full_leader, 0, brow, bcol / 64, pol_b);
           ++issued;
@@ -327,8 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sb = sa + kPairABytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bdesc = smem_desc_sw128(sb + kk * 2048, 8192, 1024);
+            // A: k-atom kk / 4 (128 rows x 128 bytes each), 16-wide slice kk % 4;
+            // B: 64-column blocks of kBK k-rows (LBO = one block), slice kk
+            const uint64_t adesc = smem_desc_sw128(sa + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t bdesc = smem_desc_sw128(sb + kk * 2048, kBK * 128, 1024);
             umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit_pair(smem_u32(&ctl.empty[stage]), 0x3);
@@ -516,10 +539,11 @@ cudaError_t make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t co
 // {64 columns, rows, cols / 64 column blocks}: a box {64, 64, nblk} holds nblk
 // consecutive 64-column blocks of 64 rows, each block 8 KB in shared memory
 // with the 128-byte swizzle; blocks past the last column read zeros.
-cudaError_t make_weight_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t nblk) {
+cudaError_t make_weight_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t nblk,
+                            uint32_t box_rows = 64) {
   cuuint64_t dims[3] = {64, rows, cols / 64};
   cuuint64_t strides[2] = {cols * 2, 128};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBK), nblk};
+  cuuint32_t box[3] = {64, box_rows, nblk};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -552,7 +576,7 @@ cudaError_t launch_pair(int nclusters, const CUtensorMap& a, const CUtensorMap& 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * nclusters, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kPairSmemBytes;
+  cfg.dynamicSmemBytes = pair_smem_bytes<kSwiGLU>();
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -582,12 +606,13 @@ cudaError_t device_setup(DeviceInfo* out) {
     for (int sw = 0; sw < 2; ++sw) {
       const void* fn = sw ? reinterpret_cast<const void*>(grouped_gemm_pair_kernel<true>)
                           : reinterpret_cast<const void*>(grouped_gemm_pair_kernel<false>);
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
+      const int smem = sw ? pair_smem_bytes<true>() : pair_smem_bytes<false>();
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * (di.sms / 2), 1, 1);
       cfg.blockDim = dim3(kThreads, 1, 1);
-      cfg.dynamicSmemBytes = kPairSmemBytes;
+      cfg.dynamicSmemBytes = smem;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = 2;
@@ -666,13 +691,14 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
   const bool shared = Ws1 != nullptr;
   const int hw = 128;  // the last tile is half empty when F % 128 == 64
   CUtensorMap mA, mAs, mB0, mB1, mB0s, mB1s;
-  if ((e = make_map(&mA, x_sorted, S, d.D, 128, kBK)) != cudaSuccess) return e;
-  if ((e = make_weight_map(&mB0, W1, static_cast<uint64_t>(d.E) * d.D, d.F, hw / 64)) != cudaSuccess) return e;
-  if ((e = make_weight_map(&mB1, W3, static_cast<uint64_t>(d.E) * d.D, d.F, hw / 64)) != cudaSuccess) return e;
+  constexpr int kBK = Ring<true>::kBK;
+  if ((e = make_weight_map(&mA, x_sorted, S, d.D, kBK / kAtomK, 128)) != cudaSuccess) return e;
+  if ((e = make_weight_map(&mB0, W1, static_cast<uint64_t>(d.E) * d.D, d.F, hw / 64, kBK)) != cudaSuccess) return e;
+  if ((e = make_weight_map(&mB1, W3, static_cast<uint64_t>(d.E) * d.D, d.F, hw / 64, kBK)) != cudaSuccess) return e;
   if (shared) {
-    if ((e = make_map(&mAs, x, d.T, d.D, 128, kBK)) != cudaSuccess) return e;
-    if ((e = make_weight_map(&mB0s, Ws1, d.D, d.F, hw / 64)) != cudaSuccess) return e;
-    if ((e = make_weight_map(&mB1s, Ws3, d.D, d.F, hw / 64)) != cudaSuccess) return e;
+    if ((e = make_weight_map(&mAs, x, d.T, d.D, kBK / kAtomK, 128)) != cudaSuccess) return e;
+    if ((e = make_weight_map(&mB0s, Ws1, d.D, d.F, hw / 64, kBK)) != cudaSuccess) return e;
+    if ((e = make_weight_map(&mB1s, Ws3, d.D, d.F, hw / 64, kBK)) != cudaSuccess) return e;
   } else {
     mAs = mA;
     mB0s = mB0;
@@ -713,10 +739,11 @@ cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uin
   const int tn = (d.D % 256 == 0) ? 256 : 128;
   const uint64_t hrows = static_cast<uint64_t>(S) + (shared ? d.T : 0);
   CUtensorMap mA, mB0, mB0s;
-  if ((e = make_map(&mA, h, hrows, d.F, 128, kBK)) != cudaSuccess) return e;
-  if ((e = make_weight_map(&mB0, W2, static_cast<uint64_t>(d.E) * d.F, d.D, tn / 128)) != cudaSuccess) return e;
+  constexpr int kBK = Ring<false>::kBK;
+  if ((e = make_weight_map(&mA, h, hrows, d.F, kBK / kAtomK, 128)) != cudaSuccess) return e;
+  if ((e = make_weight_map(&mB0, W2, static_cast<uint64_t>(d.E) * d.F, d.D, tn / 128, kBK)) != cudaSuccess) return e;
   if (shared) {
-    if ((e = make_weight_map(&mB0s, Ws2, d.F, d.D, tn / 128)) != cudaSuccess) return e;
+    if ((e = make_weight_map(&mB0s, Ws2, d.F, d.D, tn / 128, kBK)) != cudaSuccess) return e;
   } else {
     mB0s = mB0;
   }
