@@ -644,13 +644,14 @@ cudaError_t tensor_map_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64
   return make_map(m, ptr, rows, cols, box_rows, box_cols);
 }
 
-cudaError_t tensor_map_blocks(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t nblk) {
+cudaError_t tensor_map_blocks(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t nblk,
+                              uint32_t box_rows) {
   {
     std::lock_guard<std::mutex> lock(g_setup_mu);
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
   }
-  return make_weight_map(m, ptr, rows, cols, nblk);
+  return make_weight_map(m, ptr, rows, cols, nblk, box_rows);
 }
 
 cudaError_t tensor_map_f32_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,

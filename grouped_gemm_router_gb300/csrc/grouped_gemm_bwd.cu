@@ -48,10 +48,7 @@ constexpr int kMaxGroups = MOE_MAX_EXPERTS + 1;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kTileM = 256;                   // rows per pair tile
 constexpr int kTileN = 256;                   // MMA N
-constexpr int kStages = 6;                    // stage ring (the activation mode uses 5)
-constexpr int kABytes = 128 * kBK * 2;        // 16 KB: this CTA's half of A per k-block
-constexpr int kBBytes = 128 * kBK * 2;        // 16 KB: this CTA's half of B per k-block
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kStages = 6;                    // largest stage ring (mbarrier arrays)
 constexpr int kOutBoxRows = 32;
 constexpr int kOutBoxCols = 32;
 constexpr int kOutBoxBytes = kOutBoxRows * kOutBoxCols * 2;
@@ -72,13 +69,22 @@ constexpr int kMaxMyTiles = 64;
 // into near-equal chunks whose fp32 partial sums a reduction kernel adds.
 constexpr int kMaxChunkKb = 160;
 
+// k per stage of each mode: 128 for the W2 dgrad (two swizzle atoms, one 3-D
+// TMA box per operand and stage: 143 -> 141.5 us on gptoss_lite), 64 for the
+// others, whose operands stream from HBM (the weight gradients and x dgrad
+// ran slower with 128-deep stages) or whose epilogue binds (the SwiGLU
+// backward: 346 -> 353 us with two such stages).
+__host__ __device__ constexpr int bk_of(int mode) { return mode == kDgradW2 ? 128 : 64; }
+__host__ __device__ constexpr int stage_bytes_of(int mode) { return 2 * 128 * bk_of(mode) * 2; }
 // The activation mode gives each epilogue warp three output staging buffers
-// (g_bar, u_bar and h boxes rotate through them) and gives up one stage of
-// the ring for them.
-__host__ __device__ constexpr int stages_of(int mode) { return mode == kActBwd ? kStages - 1 : kStages; }
+// (g_bar, u_bar and h boxes rotate through them) and gives up ring space for
+// them.
+__host__ __device__ constexpr int stages_of(int mode) {
+  return mode == kActBwd ? (bk_of(mode) == 128 ? 2 : kStages - 1) : (bk_of(mode) == 128 ? 3 : kStages);
+}
 __host__ __device__ constexpr int out_boxes_of(int mode) { return mode == kActBwd ? 3 : 1; }
 __host__ __device__ constexpr int smem_bytes_of(int mode) {
-  return stages_of(mode) * kStageBytes + kEpiWarps * out_boxes_of(mode) * kOutBoxBytes + 1024;
+  return stages_of(mode) * stage_bytes_of(mode) + kEpiWarps * out_boxes_of(mode) * kOutBoxBytes + 1024;
 }
 
 template <int kMode>
@@ -170,6 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const __grid_constant__ CUtensorMap mapC5, const BwdArgs p) {
   using Tr = Traits<kMode>;
   constexpr int kSt = stages_of(kMode);
+  constexpr int kBKm = bk_of(kMode);             // k per stage of this mode
+  constexpr int kStageBytes = stage_bytes_of(kMode);
+  constexpr int kABytes = kStageBytes / 2;       // this CTA's half of A per stage
   extern __shared__ uint8_t bwd_smem_raw[];
   __shared__ BwdCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -433,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       t.m = local / ntn;
       t.n = local - t.m * ntn;
       t.kb0 = 0;
-      t.kb1 = p.K / kBK;
+      t.kb1 = (p.K + kBKm - 1) / kBKm;
     } else {
       const int per_chunk = nmt * ntn;
       t.c = local / per_chunk;
@@ -478,21 +487,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (Tr::row_tiles) {
             // A: 128 rows of this CTA, K-major
             const int a0 = routed ? (kMode == kActBwd ? ctl.row0[g] : ctl.prow0[g]) : 0;
-            tma_load_2d_pair(sa, mA, full_leader, kb * kBK, a0 + m * kTileM + 128 * static_cast<int>(rank),
-                             pol_a);
+            tma_load_3d_pair(sa, mA, full_leader, 0, a0 + m * kTileM + 128 * static_cast<int>(rank),
+                             kb * (kBKm / 64), pol_a);
             if (kMode == kActBwd) {
               // B = W1 (leader) / W3 (peer) columns of the tile, N-major
               const CUtensorMap* mB =
                   leader ? (routed ? &mapB0 : &mapB0_sh) : (routed ? &mapB1 : &mapB1_sh);
-              const int brow = (routed ? g * p.K : 0) + kb * kBK;
+              const int brow = (routed ? g * p.K : 0) + kb * kBKm;
               tma_load_3d_pair(sb, mB, full_leader, 0, brow, (n * hw) / 64, pol_b);
             } else {
               // B^T rows of this CTA's half of the tile's columns, K-major
-              const bool second = kMode == kDgradX && kb * kBK >= p.K1;
+              const bool second = kMode == kDgradX && kb * kBKm >= p.K1;
               const CUtensorMap* mB = second ? (routed ? &mapB1 : &mapB1_sh) : (routed ? &mapB0 : &mapB0_sh);
-              const int k0 = second ? kb * kBK - p.K1 : kb * kBK;
+              const int k0 = second ? kb * kBKm - p.K1 : kb * kBKm;
               const int brow = (routed ? g * p.b_rows : 0) + n * kTileN + half_n * static_cast<int>(rank);
-              tma_load_2d_pair(sb, mB, full_leader, k0, brow, pol_b);
+              tma_load_3d_pair(sb, mB, full_leader, 0, brow, k0 / 64, pol_b);
             }
           } else {
             // kWgrad: k = rows of the group; A [rows, M] and B [rows, N] tiles, M/N-major
@@ -550,11 +559,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = smem_base + stage * kStageBytes;
           const uint32_t sb = sa + kABytes;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t adesc = Tr::a_mn ? smem_desc_sw128(sa + kk * 2048, 8192, 1024)
-                                            : smem_desc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bdesc = Tr::b_mn ? smem_desc_sw128(sb + kk * 2048, 8192, 1024)
-                                            : smem_desc_sw128(sb + kk * 32, 16, 1024);
+          for (int kk = 0; kk < kBKm / 16; ++kk) {
+            // K-major: atom kk / 4 (128 rows x 128 bytes), 16-wide slice kk % 4;
+            // M/N-major: 64-column blocks of kBKm k-rows (LBO = one block), slice kk
+            const uint64_t adesc = Tr::a_mn ? smem_desc_sw128(sa + kk * 2048, kBKm * 128, 1024)
+                                            : smem_desc_sw128(sa + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+            const uint64_t bdesc = Tr::b_mn ? smem_desc_sw128(sb + kk * 2048, kBKm * 128, 1024)
+                                            : smem_desc_sw128(sb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
             umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb != ti.kb0 || kk != 0) ? 1u : 0u);
           }
           umma_commit_pair(smem_u32(&ctl.empty[stage]), 0x3);
@@ -1032,11 +1043,14 @@ cudaError_t launch_bwd_dgrad_w2(const BwdLayout& L, const int32_t* offsets, cons
   const uint64_t rows = static_cast<uint64_t>(L.S_pad) + (L.shared ? d.T : 0);
   CUtensorMap m[kMaps];
   cudaError_t e;
-  if ((e = tensor_map_2d(&m[0], ybar, L.S_pad, d.D, 128, kBK)) != cudaSuccess) return e;
-  if ((e = tensor_map_2d(&m[2], W2, static_cast<uint64_t>(d.E) * d.F, d.D, 128, kBK)) != cudaSuccess) return e;
+  // K-major operands as {64, rows, K / 64} block views: one box of 128 rows
+  // and a stage's 64-deep atoms per operand
+  constexpr uint32_t na = bk_of(kDgradW2) / 64;
+  if ((e = tensor_map_blocks(&m[0], ybar, L.S_pad, d.D, na, 128)) != cudaSuccess) return e;
+  if ((e = tensor_map_blocks(&m[2], W2, static_cast<uint64_t>(d.E) * d.F, d.D, na, 128)) != cudaSuccess) return e;
   if (L.shared) {
-    if ((e = tensor_map_2d(&m[1], d_out, d.T, d.D, 128, kBK)) != cudaSuccess) return e;
-    if ((e = tensor_map_2d(&m[4], Ws2, d.F, d.D, 128, kBK)) != cudaSuccess) return e;
+    if ((e = tensor_map_blocks(&m[1], d_out, d.T, d.D, na, 128)) != cudaSuccess) return e;
+    if ((e = tensor_map_blocks(&m[4], Ws2, d.F, d.D, na, 128)) != cudaSuccess) return e;
   } else {
     m[1] = m[0];
     m[4] = m[2];
@@ -1062,13 +1076,14 @@ cudaError_t launch_bwd_act(const BwdLayout& L, const int32_t* offsets, const uin
   const int S = d.T * d.k;
   CUtensorMap m[kMaps];
   cudaError_t e;
-  if ((e = tensor_map_2d(&m[0], x_sorted, S, d.D, 128, kBK)) != cudaSuccess) return e;
-  if ((e = tensor_map_blocks(&m[2], W1, static_cast<uint64_t>(d.E) * d.D, d.F, 2)) != cudaSuccess) return e;
-  if ((e = tensor_map_blocks(&m[3], W3, static_cast<uint64_t>(d.E) * d.D, d.F, 2)) != cudaSuccess) return e;
+  constexpr uint32_t kb1 = bk_of(kActBwd);
+  if ((e = tensor_map_blocks(&m[0], x_sorted, S, d.D, kb1 / 64, 128)) != cudaSuccess) return e;
+  if ((e = tensor_map_blocks(&m[2], W1, static_cast<uint64_t>(d.E) * d.D, d.F, 2, kb1)) != cudaSuccess) return e;
+  if ((e = tensor_map_blocks(&m[3], W3, static_cast<uint64_t>(d.E) * d.D, d.F, 2, kb1)) != cudaSuccess) return e;
   if (L.shared) {
-    if ((e = tensor_map_2d(&m[1], x, d.T, d.D, 128, kBK)) != cudaSuccess) return e;
-    if ((e = tensor_map_blocks(&m[4], Ws1, d.D, d.F, 2)) != cudaSuccess) return e;
-    if ((e = tensor_map_blocks(&m[5], Ws3, d.D, d.F, 2)) != cudaSuccess) return e;
+    if ((e = tensor_map_blocks(&m[1], x, d.T, d.D, kb1 / 64, 128)) != cudaSuccess) return e;
+    if ((e = tensor_map_blocks(&m[4], Ws1, d.D, d.F, 2, kb1)) != cudaSuccess) return e;
+    if ((e = tensor_map_blocks(&m[5], Ws3, d.D, d.F, 2, kb1)) != cudaSuccess) return e;
   } else {
     m[1] = m[0];
     m[4] = m[2];
@@ -1098,14 +1113,15 @@ cudaError_t launch_bwd_dgrad_x(const BwdLayout& L, const int32_t* offsets, const
   const uint64_t rows = static_cast<uint64_t>(L.S_pad) + (L.shared ? d.T : 0);
   CUtensorMap m[kMaps];
   cudaError_t e;
-  if ((e = tensor_map_2d(&m[0], gu, L.S_pad, 2 * d.F, 128, kBK)) != cudaSuccess) return e;
-  if ((e = tensor_map_2d(&m[2], W1, static_cast<uint64_t>(d.E) * d.D, d.F, 128, kBK)) != cudaSuccess) return e;
-  if ((e = tensor_map_2d(&m[3], W3, static_cast<uint64_t>(d.E) * d.D, d.F, 128, kBK)) != cudaSuccess) return e;
+  constexpr uint32_t nx = bk_of(kDgradX) / 64;
+  if ((e = tensor_map_blocks(&m[0], gu, L.S_pad, 2 * d.F, nx, 128)) != cudaSuccess) return e;
+  if ((e = tensor_map_blocks(&m[2], W1, static_cast<uint64_t>(d.E) * d.D, d.F, nx, 128)) != cudaSuccess) return e;
+  if ((e = tensor_map_blocks(&m[3], W3, static_cast<uint64_t>(d.E) * d.D, d.F, nx, 128)) != cudaSuccess) return e;
   if (L.shared) {
     const uint16_t* gu_sh = gu + static_cast<size_t>(L.S_pad) * 2 * d.F;
-    if ((e = tensor_map_2d(&m[1], gu_sh, d.T, 2 * d.F, 128, kBK)) != cudaSuccess) return e;
-    if ((e = tensor_map_2d(&m[4], Ws1, d.D, d.F, 128, kBK)) != cudaSuccess) return e;
-    if ((e = tensor_map_2d(&m[5], Ws3, d.D, d.F, 128, kBK)) != cudaSuccess) return e;
+    if ((e = tensor_map_blocks(&m[1], gu_sh, d.T, 2 * d.F, nx, 128)) != cudaSuccess) return e;
+    if ((e = tensor_map_blocks(&m[4], Ws1, d.D, d.F, nx, 128)) != cudaSuccess) return e;
+    if ((e = tensor_map_blocks(&m[5], Ws3, d.D, d.F, nx, 128)) != cudaSuccess) return e;
   } else {
     m[1] = m[0];
     m[4] = m[2];

@@ -140,11 +140,12 @@ cudaError_t launch_router_bwd(const BwdLayout& L, const uint16_t* x_sorted, cons
 cudaError_t tensor_map_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
                           uint32_t box_rows, uint32_t box_cols);
 // 3-D bf16 TMA descriptor of a row-major [rows, cols] matrix (cols % 64 == 0)
-// viewed as {64 columns, rows, cols / 64 column blocks}: a box {64, 64, nblk}
-// lands nblk consecutive 64-column blocks of 64 rows, 8 KB each with the
-// 128-byte swizzle, in one TMA operation; blocks past the last column read
-// zeros (grouped_gemm.cu).
-cudaError_t tensor_map_blocks(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t nblk);
+// viewed as {64 columns, rows, cols / 64 column blocks}: a box {64, box_rows,
+// nblk} lands nblk consecutive 64-column blocks of box_rows rows (128 bytes a
+// row, 128-byte swizzle) in one TMA operation; blocks past the last column
+// read zeros (grouped_gemm.cu).
+cudaError_t tensor_map_blocks(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t nblk,
+                              uint32_t box_rows = 64);
 // 3-D fp32 TMA descriptor of a packed [d2][d1][d0] array with a {box0, box1, 1}
 // box: 64-byte swizzle for 16-float boxes (128-byte for 32), none otherwise.
 cudaError_t tensor_map_f32_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
