@@ -8,7 +8,8 @@
 //   x_bar = g_bar W1^T + u_bar W3^T                           (x dgrad)
 //   W1_bar = x^T g_bar,  W3_bar = x^T u_bar,  W2_bar = h^T y_bar  (wgrad)
 // One persistent CTA-pair kernel (same engine as the forward grouped GEMM:
-// 256 x N pair tiles, 6 TMA stages, two TMEM accumulators, bounded waits)
+// 256 x N pair tiles, a TMA stage ring of up to 192 KB, two TMEM accumulators,
+// bounded waits)
 // runs four modes:
 //   kDgradW2  A = y_bar rows (K-major), B = W2[e]^T read K-major from the
 //             rows of W2 [E*F, D]; bf16 h_bar out.
