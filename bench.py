@@ -97,6 +97,12 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def w1w3_kernel_name(w):
+    """The W1||W3 kernel instance the library launches for this layer: it
+    stages 128 k per stage when D is a multiple of 128, 64 k otherwise."""
+    return "grouped_gemm_pair_kernel<true, true>" if w.D % 128 == 0 else "grouped_gemm_pair_kernel<true, false>"
+
+
 def ncu_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or
     None when the kernels changed since the counters were taken."""
@@ -742,7 +748,7 @@ def main():
     tokens_s = T * world / (ms / 1e3)
     w1w3_s = st_mean["w1w3"] / 1e3
     achieved = w1w3_flops_per_launch(w) / w1w3_s / 1e12
-    traffic = ncu_traffic("grouped_gemm_pair_kernel<true>")
+    traffic = ncu_traffic(w1w3_kernel_name(w))
     hbm_stages = st_mean["route"] + st_mean["permute"] + st_mean["combine"]
     hbm_bytes = sb["route"] + sb["permute"] + sb["combine"]
 
@@ -777,7 +783,7 @@ def main():
         "frac_of_datasheet_bf16_dense": fl / (ms / 1e3) / 1e12 / DATASHEET_BF16_DENSE_TFLOPS,
         "stage_ms": st_mean,
         "stage_ms_note": f"{KB} extra steps with an event at every stage boundary (serialised launches)",
-        "roofline": {"bound": "tensor", "kernel": "grouped_gemm_pair_kernel<true> (W1||W3 + SiLU*mul)",
+        "roofline": {"bound": "tensor", "kernel": w1w3_kernel_name(w) + " (W1||W3 + SiLU*mul)",
                      "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
                      "peak_kind": f"{pk_kind} bf16 burst"},

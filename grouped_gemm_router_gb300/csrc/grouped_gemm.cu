@@ -107,15 +107,17 @@ struct GemmArgs {
 // ---------------------------------------------------------------------------
 constexpr int kPairBM = 256;                  // rows per pair tile
 constexpr int kMaxPairStages = 6;
-// The stage ring of each GEMM: 192 KB per CTA either way.  W1||W3 stages
-// 128-deep k blocks (two swizzle atoms of A and of B, one TMA operation
-// each), W2 64-deep ones: halving the TMA operations per byte took W1||W3
-// from 277 to 258 us on gptoss_lite, while W2, whose A rows come from HBM,
-// ran 146 -> 149 us with three deep stages and keeps six.
-template <bool kSwiGLU>
+// The stage ring: 192 KB per CTA either way, three 128-deep stages (two
+// swizzle atoms of A and of B, one TMA operation each) or six 64-deep ones.
+// Halving the TMA operations per byte took W1||W3 from 277 to 258 us on
+// gptoss_lite; W2, whose A rows come from HBM, ran 146 -> 149 us with them.
+// So W1||W3 stages 128 k and W2 64 k -- W1||W3 too when D % 128 != 0, where
+// the last deep stage would read the next expert's W1 / W3 rows (multiplied
+// by zeros, but an inf there would still reach this expert's output).
+template <bool kDeep>
 struct Ring {
-  static constexpr int kBK = kSwiGLU ? 128 : 64;          // k per stage
-  static constexpr int kStages = kSwiGLU ? 3 : 6;
+  static constexpr int kBK = kDeep ? 128 : 64;            // k per stage
+  static constexpr int kStages = kDeep ? 3 : 6;
   static constexpr int kABytes = 128 * kBK * 2;           // this CTA's 128 rows
   static constexpr int kBBytesMax = 128 * kBK * 2;        // this CTA's half of N <= 256
   static constexpr int kStageBytes = kABytes + kBBytesMax;
@@ -132,9 +134,9 @@ struct EpiShape {
   static constexpr int kMaxBoxes = (kSwiGLU ? 128 : 256) / kEpiParts / kOutBoxCols;
   static constexpr int kAccRegs = kMaxBoxes * 32 * (kSwiGLU ? 2 : 1);
 };
-template <bool kSwiGLU>
+template <bool kDeep>
 constexpr int pair_smem_bytes() {
-  return Ring<kSwiGLU>::kStages * Ring<kSwiGLU>::kStageBytes + kEpiWarps * kOutBufs * kOutBoxBytes + 1024;
+  return Ring<kDeep>::kStages * Ring<kDeep>::kStageBytes + kEpiWarps * kOutBufs * kOutBoxBytes + 1024;
 }
 
 struct PairCtl {
@@ -151,7 +153,7 @@ struct PairCtl {
   int nrows[kMaxGroups];
 };
 
-template <bool kSwiGLU>
+template <bool kSwiGLU, bool kDeep>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA,
                              const __grid_constant__ CUtensorMap mapA_sh,
@@ -175,10 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.E + (p.T_shared > 0 ? 1 : 0);
   const int hw = kSwiGLU ? p.tile_n / 2 : p.tile_n;  // output columns per tile
   const int ntn = (p.N + hw - 1) / hw;
-  constexpr int kBK = Ring<kSwiGLU>::kBK;
-  constexpr int kPairStages = Ring<kSwiGLU>::kStages;
-  constexpr int kPairABytes = Ring<kSwiGLU>::kABytes;
-  constexpr int kPairStageBytes = Ring<kSwiGLU>::kStageBytes;
+  constexpr int kBK = Ring<kDeep>::kBK;
+  constexpr int kPairStages = Ring<kDeep>::kStages;
+  constexpr int kPairABytes = Ring<kDeep>::kABytes;
+  constexpr int kPairStageBytes = Ring<kDeep>::kStageBytes;
   const int nkb = (p.K + kBK - 1) / kBK;  // a K of 64 mod 128 reads zeros past D (TMA fill)
   const int half_n = p.tile_n / 2;                    // B columns staged by this CTA
   constexpr int kMaxBoxes = EpiShape<kSwiGLU>::kMaxBoxes;
@@ -563,12 +565,12 @@ int max_pair_tiles(long rows, int groups, int ntn) {
 struct DeviceInfo {
   int device = -1;
   int sms = 0;
-  int pair_clusters[2] = {0, 0};  // co-resident CTA pairs: [down, swiglu]
+  int pair_clusters[3] = {0, 0, 0};  // co-resident CTA pairs: [down, swiglu, swiglu deep]
   bool attrs_set = false;
 };
 DeviceInfo g_dev[64];
 
-template <bool kSwiGLU>
+template <bool kSwiGLU, bool kDeep>
 cudaError_t launch_pair(int nclusters, const CUtensorMap& a, const CUtensorMap& as,
                         const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b0s,
                         const CUtensorMap& b1s, const CUtensorMap& c, const CUtensorMap& cs,
@@ -576,7 +578,7 @@ cudaError_t launch_pair(int nclusters, const CUtensorMap& a, const CUtensorMap& 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * nclusters, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = pair_smem_bytes<kSwiGLU>();
+  cfg.dynamicSmemBytes = pair_smem_bytes<kDeep>();
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -587,7 +589,7 @@ cudaError_t launch_pair(int nclusters, const CUtensorMap& a, const CUtensorMap& 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kSwiGLU>, a, as, b0, b1, b0s, b1s, c, cs, args);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kSwiGLU, kDeep>, a, as, b0, b1, b0s, b1s, c, cs, args);
 }
 
 // One-time set-up of the current device (kernel attributes, co-resident
@@ -603,10 +605,12 @@ cudaError_t device_setup(DeviceInfo* out) {
   if (!di.attrs_set) {
     e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    for (int sw = 0; sw < 2; ++sw) {
-      const void* fn = sw ? reinterpret_cast<const void*>(grouped_gemm_pair_kernel<true>)
-                          : reinterpret_cast<const void*>(grouped_gemm_pair_kernel<false>);
-      const int smem = sw ? pair_smem_bytes<true>() : pair_smem_bytes<false>();
+    // [0] W2, [1] W1||W3 with 64-deep stages, [2] W1||W3 with 128-deep stages
+    for (int sw = 0; sw < 3; ++sw) {
+      const void* fn = sw == 2   ? reinterpret_cast<const void*>(grouped_gemm_pair_kernel<true, true>)
+                       : sw == 1 ? reinterpret_cast<const void*>(grouped_gemm_pair_kernel<true, false>)
+                                 : reinterpret_cast<const void*>(grouped_gemm_pair_kernel<false, false>);
+      const int smem = sw == 2 ? pair_smem_bytes<true>() : pair_smem_bytes<false>();
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
       cudaLaunchConfig_t cfg = {};
@@ -692,7 +696,8 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
   const bool shared = Ws1 != nullptr;
   const int hw = 128;  // the last tile is half empty when F % 128 == 64
   CUtensorMap mA, mAs, mB0, mB1, mB0s, mB1s;
-  constexpr int kBK = Ring<true>::kBK;
+  const bool deep = d.D % 128 == 0;
+  const int kBK = deep ? Ring<true>::kBK : Ring<false>::kBK;
   if ((e = make_weight_map(&mA, x_sorted, S, d.D, kBK / kAtomK, 128)) != cudaSuccess) return e;
   if ((e = make_weight_map(&mB0, W1, static_cast<uint64_t>(d.E) * d.D, d.F, hw / 64, kBK)) != cudaSuccess) return e;
   if ((e = make_weight_map(&mB1, W3, static_cast<uint64_t>(d.E) * d.D, d.F, hw / 64, kBK)) != cudaSuccess) return e;
@@ -721,9 +726,10 @@ cudaError_t launch_grouped_swiglu(const uint16_t* x_sorted, const uint16_t* x, c
       cudaSuccess)
     return e;
   const int groups1 = d.E + (shared ? 1 : 0);
-  const int pairs1 = std::min(di.pair_clusters[1],
+  const int pairs1 = std::min(di.pair_clusters[deep ? 2 : 1],
                               max_pair_tiles(static_cast<long>(S) + (shared ? d.T : 0), groups1, (d.F + hw - 1) / hw));
-  e = launch_pair<true>(pairs1, mA, mAs, mB0, mB1, mB0s, mB1s, mC, mC, a, s, pdl);
+  e = deep ? launch_pair<true, true>(pairs1, mA, mAs, mB0, mB1, mB0s, mB1s, mC, mC, a, s, pdl)
+           : launch_pair<true, false>(pairs1, mA, mAs, mB0, mB1, mB0s, mB1s, mC, mC, a, s, pdl);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -769,7 +775,7 @@ cudaError_t launch_grouped_down(const uint16_t* h, const uint16_t* W2, const uin
   const int groups0 = d.E + (shared ? 1 : 0);
   const int pairs0 = std::min(di.pair_clusters[0],
                               max_pair_tiles(static_cast<long>(S) + (shared ? d.T : 0), groups0, (d.D + tn - 1) / tn));
-  e = launch_pair<false>(pairs0, mA, mA, mB0, mB0, mB0s, mB0s, mC, mCs, a, s, pdl);
+  e = launch_pair<false, false>(pairs0, mA, mA, mB0, mB0, mB0s, mB0s, mC, mCs, a, s, pdl);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }

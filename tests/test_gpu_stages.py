@@ -191,6 +191,30 @@ def test_grouped_gemms(moe, case):
     assert moe.device_error() == 0
 
 
+@pytest.mark.parametrize("D", [192, 256])
+def test_expert_weights_do_not_reach_other_experts(moe, D):
+    """Each expert's h depends on its own W1 / W3 rows only: with an inf in
+    every row of the next expert's W1 and W3, the rows of expert 0 still match
+    the oracle (D = 192 is not a multiple of the 128-deep W1||W3 stage, so it
+    stages 64 k; D = 256 stages 128 k)."""
+    T, F, E, k = 300, 256, 4, 2
+    w_, L = _layer(T, D, F, E, k, False, 18)
+    ids, w, pm, xs_bits = _grouped_inputs(L, k, E)
+    W1, W3 = L["W1"].copy(), L["W3"].copy()
+    inf_bits = np.uint16(0x7F80)  # bf16 +inf
+    W1[1, :, 0] = inf_bits
+    W3[1, :, 0] = inf_bits
+    h = moe.moe_grouped_swiglu(to_dev(xs_bits), to_dev(pm["offsets"]), to_dev(W1), to_dev(W3), T, k)
+    torch.cuda.synchronize()
+    o0, o1 = int(pm["offsets"][0]), int(pm["offsets"][1])
+    assert o1 > o0
+    h_ref = orc.grouped_swiglu(orc.bf16_to_f64(xs_bits[o0:o1]), orc.bf16_to_f64(L["W1"][:1]),
+                               orc.bf16_to_f64(L["W3"][:1]), np.array([0, o1 - o0], dtype=np.int64))
+    h0 = to_f64(h)[o0:o1]
+    assert np.isfinite(h0).all()
+    assert_close(h0, h_ref, "h of expert 0", atol=H_ATOL, rtol=H_RTOL)
+
+
 def test_combine_exact_small(moe):
     """Combine with y values and weights that are exact in bf16/fp32: the
     fp32 sum is exact, so the bf16 output equals the rounded fp64 sum."""
